@@ -1,0 +1,343 @@
+"""Benchmark: MoE FusedDispatch + FusedCombine on one GB300 (per rank).
+
+One step = one pass of the whole hot path over one batch: moe_plan (top-k,
+gates, replica map, histogram, scan, slots) -> moe_dispatch (INT8 quantize +
+scatter into k expert slots) -> moe_combine (gate-weighted gather-reduce),
+at 4096 tokens x hidden 7168, 256 experts + 32 redundant replicas (288
+physical), top-8.  Expert outputs are synthetic bf16 rows resident in the
+pool's combine buffers.  Consecutive steps alternate the two buffer sets.
+
+Prints ONE JSON line (rank 0).  `value` is tokens/s with inputs already in
+HBM; `e2e` is the same metric through moe_step_host with pinned host buffers
+(host->device copies of logits, x and expert outputs, device->host copy of y
+inside the timed region).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the only other implementation of this
+path) on the host cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_moe_plan_gb300 import workloads as wl  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    return FALLBACK_HBM_GBS, "fallback (earlier GB300 copy measurement)"
+
+
+def _traffic(kernel_file: str, kernel: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel's
+    source has not changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    src = open(os.path.join(ROOT, "combine_moe_plan_gb300", "csrc", kernel_file), "rb").read()
+    if hashlib.sha256(src).hexdigest() != d.get("source_sha256"):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 9]
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.strip() == "Active"})
+        # samples under load: SM clock above the idle floor
+        load = [s for s in sm if s > 0.5 * (max(sm) if sm else 1)]
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _oracle_step_fn(w: wl.Workload, inp: dict):
+    """A function running the oracle over tokens [a, b) of the workload."""
+    import oracle
+    oracle.build()
+
+    def run(a, b):
+        ex = inp["ex_out"][: (b - a) * w.k] if "ex_out" in inp else None
+        oracle.forward(inp["logits"][a:b], inp["x"][a:b], w.k, inp["rep_off"], inp["rep_ids"], w.P, ex_out=ex)
+    return run
+
+
+def cpu_baseline(w: wl.Workload, inp: dict, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands on one host core, on a bounded sample of the
+    workload: whole batches while they fit the budget, else a token prefix."""
+    run = _oracle_step_fn(w, inp)
+    t0 = time.perf_counter()
+    run(0, min(w.T, 64))
+    per_tok = (time.perf_counter() - t0) / min(w.T, 64)
+    n_tok = int(max(64, min(w.T, budget_s / max(per_tok, 1e-9))))
+    reps = max(1, int(budget_s / (per_tok * n_tok)))
+    reps = min(reps, 3)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        run(0, n_tok)
+    dt = time.perf_counter() - t0
+    return {"value": reps * n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} x the first {n_tok} tokens of {w.name} (plan+dispatch+combine, single thread)"}
+
+
+def run_reference(a, w: wl.Workload):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    inp = wl.make_inputs(w)
+    run = _oracle_step_fn(w, inp)
+    t0 = time.perf_counter()
+    run(0, 32)
+    per_tok = (time.perf_counter() - t0) / 32
+    budget = 90.0  # seconds for warmup + timed steps
+    n_tok = int(max(1, min(w.T, budget / max(1, a.steps + a.warmup) / max(per_tok, 1e-9))))
+    for _ in range(a.warmup):
+        run(0, n_tok)
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        run(0, n_tok)
+    dt = time.perf_counter() - t0
+    v = a.steps * n_tok / dt
+    sample = f"first {n_tok} tokens of {w.name} per step (plan+dispatch+combine, single thread)"
+    print(json.dumps({
+        "impl": "reference", "metric": "dispatch+combine tokens/s (plan+dispatch+combine per step)",
+        "value": v, "unit": "tokens/s", "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8+bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens_per_step": n_tok, "H": w.H, "E": w.E, "P": w.P, "k": w.k},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(a, w: wl.Workload):
+    import torch
+    import torch.distributed as dist
+
+    from combine_moe_plan_gb300 import build as moe_build
+    from combine_moe_plan_gb300 import moe
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    moe_build.build()
+    moe.lib()
+
+    # ---- inputs (seed = rank: each rank its own batch; weak scaling) ----
+    inp = wl.make_inputs(w, seed=rank)
+    dev = torch.device("cuda", local)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    ex_host = torch.from_numpy(inp["ex_out"].view(np.int16)).view(torch.bfloat16)
+    rep_off = None if inp["rep_off"] is None else torch.from_numpy(inp["rep_off"]).to(dev)
+    rep_ids = None if inp["rep_ids"] is None else torch.from_numpy(inp["rep_ids"]).to(dev)
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2, device=dev)
+    for b in range(2):
+        pool.view(b)["ex_out"][: w.rows].copy_(ex_host.to(dev))
+    ys = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        b = i & 1
+        if ev is not None:
+            ev[0].record(stream)
+        pool.plan(logits, rep_off, rep_ids, buf=b)
+        if ev is not None:
+            ev[1].record(stream)
+        pool.dispatch(x, buf=b)
+        if ev is not None:
+            ev[2].record(stream)
+        pool.combine(w.T, y=ys[b], buf=b)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for i in range(a.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if pool.check() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- device-resident timed region ----
+    n_ev = min(a.steps, 400)  # per-kernel events on a subset of steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = pool.launches()
+    t_start.record(stream)
+    ev_stride = max(1, a.steps // n_ev)
+    k_ev = 0
+    for i in range(a.steps):
+        use = (i % ev_stride == 0) and k_ev < n_ev
+        step(a.warmup + i, evs[k_ev] if use else None)
+        k_ev += int(use)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    launches = pool.launches() - launches0
+    ms = t_start.elapsed_time(t_end) / a.steps
+    err = pool.check()
+    if err != 0:
+        raise RuntimeError(f"device error word {err:#x}")
+    per = {"plan": [], "dispatch": [], "combine": []}
+    for e in evs[:k_ev]:
+        per["plan"].append(e[0].elapsed_time(e[1]))
+        per["dispatch"].append(e[1].elapsed_time(e[2]))
+        per["combine"].append(e[2].elapsed_time(e[3]))
+    per_us = {k: 1e3 * statistics.median(v) for k, v in per.items()}
+    mean_us = {k: 1e3 * statistics.fmean(v) for k, v in per.items()}
+
+    # ---- e2e: whole layer from pinned host buffers through moe_step_host ----
+    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+    h_x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_ex = ex_host.pin_memory()
+    h_y = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    for i in range(3):
+        pool.step_host(h_logits, h_x, h_y, h_ex, rep_off, rep_ids, buf=i & 1)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    e0.record(stream)
+    for i in range(a.e2e_steps):
+        pool.step_host(h_logits, h_x, h_y, h_ex, rep_off, rep_ids, buf=i & 1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
+    if not torch.equal(h_y, ys[(a.warmup + a.steps - 1) & 1].cpu()):
+        raise RuntimeError("moe_step_host output differs from the device-resident path")
+
+    # ---- max over ranks ----
+    if ws > 1:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+
+    if rank == 0:
+        bytes_ = w.algorithmic_bytes()
+        peak, peak_src = _peaks()
+        comb_s = mean_us["combine"] * 1e-6
+        achieved = bytes_["combine"] / comb_s / 1e9
+        traffic = _traffic("combine.cu", "combine_kernel")
+        tokens = w.T * ws
+        out = {
+            "metric": "dispatch+combine tokens/s (plan+dispatch+combine per step)",
+            "value": tokens / (ms * 1e-3), "unit": "tokens/s", "n_gpus": ws, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8+bf16 (fp32 accumulate)",
+            "data": "synthetic (seeded; N(0,1) logits + Zipf(1.2) expert bias, N(0,1) bf16 x and expert outputs)",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "P": w.P, "k": w.k,
+                       "group": w.group, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2 (about 0.83 GB touched per step, two buffer sets alternate)"},
+            "us_per_call": {"plan": per_us["plan"], "dispatch": per_us["dispatch"],
+                            "combine": per_us["combine"], "step": ms * 1e3},
+            "hbm_gbs": {"step": bytes_["total"] / (ms * 1e-3) / 1e9,
+                        "dispatch": bytes_["dispatch"] / (per_us["dispatch"] * 1e-6) / 1e9,
+                        "combine": bytes_["combine"] / (per_us["combine"] * 1e-6) / 1e9,
+                        "step_frac_of_peak": bytes_["total"] / (ms * 1e-3) / 1e9 / peak},
+            "algorithmic_bytes": bytes_,
+            "roofline": {"kernel": "combine_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": peak_src},
+            "e2e": {"value": w.T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(inp["logits"].nbytes + inp["x"].nbytes + inp["ex_out"].nbytes),
+                    "d2h_bytes_per_step": int(w.T * w.H * 2), "ms_per_step": e2e_ms},
+            "gpu_launches": int(launches),
+            "clocks": clocks,
+        }
+        if not a.no_cpu_baseline and ws == 1:
+            out["cpu_baseline"] = cpu_baseline(w, inp)
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    a = _args()
+    w = wl.WORKLOADS[a.workload]
+    if a.impl == "reference":
+        run_reference(a, w)
+    else:
+        run_ours(a, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,153 @@
+// dispatch.cu -- FusedDispatch data phase: per-token INT8 quantization with
+// one fp32 scale per 128 elements, scattered into the token's k expert slots.
+//
+// CloudMatrix384 write-up, "FusedDispatch and FusedCombine": early INT8
+// quantization before the data moves (14 KB bf16 -> about 7.5 KB per token
+// with its scales), direct writes into pre-allocated receive buffers, and a
+// token-level pipeline of load -> quantize/address -> write.
+//
+// GPU mapping: one warp per (token, 512-element segment).  Each lane loads 16
+// bf16 values (two 16-byte loads), a group of 128 elements spans 8 lanes, so
+// amax is a 3-step xor-shuffle; codes are rint((x * 127) / amax) with IEEE
+// fp32 division and round-half-even conversion; the lane's 16 codes leave as
+// one 16-byte store into each of the token's k rows; the 4 group scales of
+// the segment leave as one 16-byte store per row.  Reads of x are streamed
+// once; every byte of every destination row is written exactly once.
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kDispatchThreads = 256;  // 8 warps, 8 (token, segment) items per CTA
+constexpr int kSegElems = 512;         // 32 lanes x 16 elements
+
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float amax) {
+    // amax == 0 only when the whole group is +-0: dividing by 1 keeps codes 0.
+    const float den = amax > 0.0f ? amax : 1.0f;
+    const int qa = __float2int_rn((a * 127.0f) / den);
+    const int qb = __float2int_rn((b * 127.0f) / den);
+    const int qc = __float2int_rn((c * 127.0f) / den);
+    const int qd = __float2int_rn((d * 127.0f) / den);
+    return (uint32_t)(qa & 0xff) | ((uint32_t)(qb & 0xff) << 8) | ((uint32_t)(qc & 0xff) << 16) |
+           ((uint32_t)(qd & 0xff) << 24);
+}
+
+__global__ void __launch_bounds__(kDispatchThreads)
+dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ slot,
+                int8_t* __restrict__ codes, float* __restrict__ scales, int Gs, int32_t* __restrict__ err) {
+    const int lane = threadIdx.x & 31;
+    const int segs = (H + kSegElems - 1) / kSegElems;
+    const long long item = (long long)blockIdx.x * (kDispatchThreads / 32) + (threadIdx.x >> 5);
+    const int t = (int)(item / segs);
+    const int seg = (int)(item - (long long)t * segs);
+    if (t >= T) return;
+
+    const int chunk = seg * 32 + lane;  // 16-element chunk within the row
+    const bool active = chunk * 16 < H;
+    const int rows = T * k;
+
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+    if (active) {
+        const uint16_t* src = x + (size_t)t * H + (size_t)chunk * 16;
+        lo = ld_stream16(src);
+        hi = ld_stream16(src + 8);
+    }
+    const int my_slot = (lane < k) ? slot[(size_t)t * k + lane] : 0;
+
+    float v[16];
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_lo(w[i]);
+        v[2 * i + 1] = bf16_hi(w[i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+
+    uint4 q;
+    q.x = quant4(v[0], v[1], v[2], v[3], amax);
+    q.y = quant4(v[4], v[5], v[6], v[7], amax);
+    q.z = quant4(v[8], v[9], v[10], v[11], amax);
+    q.w = quant4(v[12], v[13], v[14], v[15], amax);
+
+    const float scale = amax / 127.0f;
+    float4 sc;
+    sc.x = __shfl_sync(kFull, scale, 0);
+    sc.y = __shfl_sync(kFull, scale, 8);
+    sc.z = __shfl_sync(kFull, scale, 16);
+    sc.w = __shfl_sync(kFull, scale, 24);
+
+    for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(kFull, my_slot, j);
+        if (r < 0 || r >= rows) {  // warp-uniform
+            if (lane == 0) set_error(err, MOE_DEVERR_SLOT);
+            continue;
+        }
+        if (active) st16(codes + (size_t)r * H + (size_t)chunk * 16, q);
+    }
+    // Scales of this segment's 4 groups: one 16-byte store per destination row.
+    if (lane < k && my_slot >= 0 && my_slot < rows && seg * 4 < Gs)
+        *reinterpret_cast<float4*>(scales + (size_t)my_slot * Gs + seg * 4) = sc;
+}
+
+constexpr int kExpertThreads = 256;
+
+// ex_out[r, i] = bf16(code[r, i] * scale[r, i / 128]); one thread per 16 codes.
+__global__ void __launch_bounds__(kExpertThreads)
+identity_experts_kernel(const int8_t* __restrict__ codes, const float* __restrict__ scales, int rows, int H,
+                        int Gs, uint16_t* __restrict__ ex_out) {
+    const int per_row = H / 16;
+    const long long n = (long long)rows * per_row;
+    for (long long c = (long long)blockIdx.x * kExpertThreads + threadIdx.x; c < n;
+         c += (long long)gridDim.x * kExpertThreads) {
+        const int r = (int)(c / per_row);
+        const int ch = (int)(c - (long long)r * per_row);
+        const uint4 q = ld_stream16(codes + (size_t)r * H + (size_t)ch * 16);
+        const float s = scales[(size_t)r * Gs + (ch * 16) / kGroup];
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float a = (float)(int8_t)(qw[i] & 0xff) * s;
+            const float b = (float)(int8_t)((qw[i] >> 8) & 0xff) * s;
+            const float c2 = (float)(int8_t)((qw[i] >> 16) & 0xff) * s;
+            const float d = (float)(int8_t)(qw[i] >> 24) * s;
+            o[2 * i] = pack_bf16x2_rn(a, b);
+            o[2 * i + 1] = pack_bf16x2_rn(c2, d);
+        }
+        uint16_t* dst = ex_out + (size_t)r * H + (size_t)ch * 16;
+        st16(dst, make_uint4(o[0], o[1], o[2], o[3]));
+        st16(dst + 8, make_uint4(o[4], o[5], o[6], o[7]));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const uint16_t* x, int T, int H, int k, const int32_t* slot, int8_t* codes,
+                            float* scales, int Gs, int32_t* err, cudaStream_t s, uint64_t* launches) {
+    const long long items = (long long)T * ((H + kSegElems - 1) / kSegElems);
+    const long long blocks = (items + (kDispatchThreads / 32) - 1) / (kDispatchThreads / 32);
+    dispatch_kernel<<<(unsigned)blocks, kDispatchThreads, 0, s>>>(x, T, H, k, slot, codes, scales, Gs, err);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) *launches += 1;
+    return e;
+}
+
+cudaError_t launch_identity_experts(const int8_t* codes, const float* scales, int rows, int H, int Gs,
+                                    uint16_t* ex_out, cudaStream_t s, uint64_t* launches) {
+    const long long n = (long long)rows * (H / 16);
+    long long blocks = (n + kExpertThreads - 1) / kExpertThreads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    identity_experts_kernel<<<(unsigned)blocks, kExpertThreads, 0, s>>>(codes, scales, rows, H, Gs, ex_out);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) *launches += 1;
+    return e;
+}
+
+}  // namespace moe

@@ -1,0 +1,65 @@
+// moe_internal.h -- pool layout and kernel launchers shared inside libmoe.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kGroup = 128;       // quantization group (elements)
+constexpr int kTileTokens = 32;   // tokens per placement tile (one mask word)
+constexpr int kMaxSets = 4;
+
+// Byte offsets (from the workspace base) of one buffer set's regions.
+struct SetLayout {
+    size_t codes, scales, ex_out;
+    size_t topk_e, phys, gates, slot, src_token, src_k, counts, offsets;
+    size_t tile_hist, local_rank;
+    size_t x_stage, logits_stage, y_stage;
+};
+
+struct Geometry {
+    moe_desc d;
+    int64_t rows;        // T_max * k
+    int32_t G;           // H / 128
+    int32_t Gs;          // G rounded up to a multiple of 4 (16-byte scale rows)
+    int32_t tiles_max;   // ceil(T_max / kTileTokens)
+    size_t error_word;   // offset of the shared device error word
+    SetLayout set[kMaxSets];
+    size_t total;
+};
+
+int make_geometry(const moe_desc* d, Geometry* g);
+
+// Launchers: enqueue on `s`, return cudaGetLastError() after the launch(es).
+// Each adds the number of kernels it launched to *launches.
+cudaError_t launch_plan(const float* logits, int T, int E, int P, int k,
+                        const int32_t* rep_off, const int32_t* rep_ids,
+                        int32_t* topk_e, float* gates, int32_t* phys,
+                        int32_t* tile_hist, int32_t* local_rank,
+                        int32_t* counts, int32_t* offsets, int32_t* slot,
+                        int32_t* src_token, int32_t* src_k, int32_t* err,
+                        cudaStream_t s, uint64_t* launches);
+
+cudaError_t launch_dispatch(const uint16_t* x, int T, int H, int k, const int32_t* slot,
+                            int8_t* codes, float* scales, int Gs, int32_t* err,
+                            cudaStream_t s, uint64_t* launches);
+
+cudaError_t launch_identity_experts(const int8_t* codes, const float* scales, int rows, int H, int Gs,
+                                    uint16_t* ex_out, cudaStream_t s, uint64_t* launches);
+
+cudaError_t launch_combine(const uint16_t* ex_out, const int32_t* slot, const float* gates,
+                           int T, int H, int k, uint16_t* y, int32_t* err,
+                           cudaStream_t s, uint64_t* launches);
+
+}  // namespace moe
+
+struct moe_pool {
+    moe::Geometry geo;
+    char* base;                       // device workspace
+    int32_t planned_T[moe::kMaxSets]; // T of the last moe_plan per set (0 = none)
+    uint64_t launches;
+};

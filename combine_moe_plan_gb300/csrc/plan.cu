@@ -1,0 +1,308 @@
+// plan.cu -- routing metadata for FusedDispatch: top-k, gates, replica pick,
+// per-expert histogram, exclusive scan and stable slot assignment.
+//
+// CloudMatrix384 write-up: "FusedDispatch and FusedCombine" (routing metadata
+// is the first of the three exchanges the fused operators absorb), "Decode
+// Phase" (redundant experts for load balancing), "Prefill Phase" (metadata
+// generation and token reordering before dispatch).  StrataCL analysis,
+// section 3.5: token placement -> expert-window aggregation.
+//
+// Three launches:
+//   route_tile   one CTA per tile of 32 tokens.  A warp finds a token's top-k
+//                with k rounds of shuffle arg-max (ties -> lower expert id),
+//                then the CTA computes gates in fp64 (batched over the
+//                tile's (token, j) pairs), applies the replica map, and sets
+//                bit t of a shared-memory mask per physical expert.  From the
+//                mask: the tile's count per expert (popc) and each copy's rank
+//                among earlier tokens of the tile (popc of the lower bits).
+//   column_scan  one warp per physical expert: exclusive scan of the tile
+//                counts down the tiles -> per-tile base inside the expert's
+//                window; the column total is counts[p].
+//   assign       every CTA scans counts[] in shared memory (offsets); each
+//                thread places one (t, j): slot = offsets[p] + tile base +
+//                in-tile rank, and writes the inverse map.
+// No atomics decide any position, so the result is deterministic and equal
+// to a stable counting sort by (expert, token).
+#include <cfloat>
+#include <climits>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;                 // 8 warps
+constexpr int kTokensPerWarp = kTileTokens / 8;    // 4
+
+template <int EPL>  // logits per lane = ceil(E / 32)
+__global__ void __launch_bounds__(kRouteThreads)
+route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
+                  const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
+                  int32_t* __restrict__ topk_e, float* __restrict__ gates,
+                  int32_t* __restrict__ phys, int32_t* __restrict__ tile_hist, int n_tiles,
+                  int32_t* __restrict__ local_rank, int32_t* __restrict__ err) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    double* e64 = reinterpret_cast<double*>(smem);                       // [32*k]
+    float* sel_v = reinterpret_cast<float*>(e64 + kTileTokens * k);      // [32*k]
+    int32_t* sel_e = reinterpret_cast<int32_t*>(sel_v + kTileTokens * k); // [32*k]
+    int32_t* sel_p = sel_e + kTileTokens * k;                            // [32*k]
+    uint32_t* mask = reinterpret_cast<uint32_t*>(sel_p + kTileTokens * k); // [P]
+
+    const int tile = blockIdx.x;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int t0 = tile * kTileTokens;
+
+    for (int p = threadIdx.x; p < P; p += kRouteThreads) mask[p] = 0u;
+
+    // ---- top-k: one warp per token ----
+    for (int i = 0; i < kTokensPerWarp; ++i) {
+        const int tl = warp * kTokensPerWarp + i;
+        const int t = t0 + tl;
+        if (t >= T) break;
+        const float* row = logits + (size_t)t * E;
+        float v[EPL];
+#pragma unroll
+        for (int r = 0; r < EPL; ++r) {
+            const int e = r * 32 + lane;
+            v[r] = (e < E) ? __ldg(row + e) : -INFINITY;
+        }
+        uint32_t taken = 0u;
+        for (int j = 0; j < k; ++j) {
+            float bv = -INFINITY;
+            int bi = INT_MAX;
+#pragma unroll
+            for (int r = 0; r < EPL; ++r) {
+                const int e = r * 32 + lane;
+                const bool ok = (e < E) && !((taken >> r) & 1u);
+                if (ok && (v[r] > bv || (v[r] == bv && e < bi))) {
+                    bv = v[r];
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(kFull, bv, off);
+                const int oi = __shfl_xor_sync(kFull, bi, off);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (bi >= E) bi = 0;  // only reachable with NaN logits (outside the domain)
+            if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+            if (lane == 0) {
+                sel_v[tl * k + j] = bv;
+                sel_e[tl * k + j] = bi;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- gates (fp64, rounded once), replica pick, mask ----
+    const int n_items = kTileTokens * k;
+    for (int it = threadIdx.x; it < n_items; it += kRouteThreads) {
+        const int tl = it / k;
+        if (t0 + tl < T) e64[it] = exp((double)sel_v[it] - (double)sel_v[tl * k]);
+    }
+    __syncthreads();
+    for (int it = threadIdx.x; it < n_items; it += kRouteThreads) {
+        const int tl = it / k;
+        const int j = it - tl * k;
+        const int t = t0 + tl;
+        if (t >= T) continue;
+        double s = 0.0;
+        for (int jj = 0; jj < k; ++jj) s += e64[tl * k + jj];
+        const float g = (float)(e64[it] / s);
+        const int e = sel_e[it];
+        int p = e;
+        if (rep_off != nullptr) {
+            const int lo = rep_off[e];
+            const int n = rep_off[e + 1] - lo;
+            if (n < 1 || lo < 0 || lo + n > P) {
+                p = -1;
+            } else {
+                p = rep_ids[lo + t % n];
+                if (p < 0 || p >= P) p = -1;
+            }
+            if (p < 0) set_error(err, MOE_DEVERR_REPLICA);
+        }
+        const size_t o = (size_t)t * k + j;
+        topk_e[o] = e;
+        gates[o] = g;
+        phys[o] = p;
+        sel_p[it] = p;
+        if (p >= 0) {
+            const uint32_t bit = 1u << tl;
+            const uint32_t old = atomicOr(&mask[p], bit);
+            if (old & bit) set_error(err, MOE_DEVERR_DUPLICATE);
+        }
+    }
+    __syncthreads();
+
+    // ---- tile histogram (expert-major) and in-tile ranks ----
+    for (int p = threadIdx.x; p < P; p += kRouteThreads)
+        tile_hist[(size_t)p * n_tiles + tile] = __popc(mask[p]);
+    for (int it = threadIdx.x; it < n_items; it += kRouteThreads) {
+        const int tl = it / k;
+        const int t = t0 + tl;
+        if (t >= T) continue;
+        const int p = sel_p[it];
+        local_rank[(size_t)t * k + (it - tl * k)] =
+            (p >= 0) ? __popc(mask[p] & ((1u << tl) - 1u)) : 0;
+    }
+}
+
+// One warp per physical expert p: exclusive scan of tile_hist[p, :] in place,
+// counts[p] = column total.
+constexpr int kScanThreads = 256;
+constexpr int kScanBatch = 8;  // chunks of 32 tiles loaded before scanning
+
+__global__ void __launch_bounds__(kScanThreads)
+column_scan_kernel(int32_t* __restrict__ tile_hist, int n_tiles, int P, int32_t* __restrict__ counts) {
+    const int p = blockIdx.x * (kScanThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (p >= P) return;
+    int32_t* col = tile_hist + (size_t)p * n_tiles;
+    int carry = 0;
+    for (int base = 0; base < n_tiles; base += 32 * kScanBatch) {
+        int v[kScanBatch];
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) {
+            const int idx = base + u * 32 + lane;
+            v[u] = (idx < n_tiles) ? col[idx] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) {
+            int incl = v[u];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(kFull, incl, off);
+                if (lane >= off) incl += o;
+            }
+            const int idx = base + u * 32 + lane;
+            if (idx < n_tiles) col[idx] = carry + incl - v[u];
+            carry += __shfl_sync(kFull, incl, 31);
+        }
+    }
+    if (lane == 0) counts[p] = carry;
+}
+
+// Exclusive scan of counts[0..P) into offs[0..P] in shared memory (whole CTA).
+template <int THREADS>
+__device__ void block_offsets(const int32_t* __restrict__ counts, int P, int32_t* offs) {
+    __shared__ int32_t warp_tot[THREADS / 32];
+    const int per = (P + THREADS - 1) / THREADS;
+    const int lo = threadIdx.x * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i)
+        if (lo + i < P) local += counts[lo + i];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+    int run = wbase + incl - local;
+    for (int i = 0; i < per; ++i) {
+        if (lo + i < P) {
+            offs[lo + i] = run;
+            run += counts[lo + i];
+        }
+    }
+    if (threadIdx.x == THREADS - 1) offs[P] = wbase + incl;
+    __syncthreads();
+}
+
+constexpr int kAssignThreads = 256;
+
+__global__ void __launch_bounds__(kAssignThreads)
+assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile_hist, int n_tiles,
+              const int32_t* __restrict__ local_rank, const int32_t* __restrict__ counts, int T, int P,
+              int k, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
+              int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err) {
+    extern __shared__ int32_t offs[];  // [P+1]
+    block_offsets<kAssignThreads>(counts, P, offs);
+    if (blockIdx.x == 0)
+        for (int p = threadIdx.x; p <= P; p += kAssignThreads) offsets[p] = offs[p];
+    const int n = T * k;
+    const int it = blockIdx.x * kAssignThreads + threadIdx.x;
+    if (it >= n) return;
+    const int t = it / k;
+    const int j = it - t * k;
+    const int p = phys[it];
+    int r = -1;
+    if (p >= 0 && p < P) r = offs[p] + tile_hist[(size_t)p * n_tiles + t / kTileTokens] + local_rank[it];
+    if (r < 0 || r >= n) {
+        set_error(err, MOE_DEVERR_SLOT);
+        slot[it] = -1;
+        return;
+    }
+    slot[it] = r;
+    src_token[r] = t;
+    src_k[r] = j;
+}
+
+template <int EPL>
+cudaError_t launch_route(dim3 grid, size_t smem, cudaStream_t s, const float* logits, int T, int E,
+                         int P, int k, const int32_t* rep_off, const int32_t* rep_ids, int32_t* topk_e,
+                         float* gates, int32_t* phys, int32_t* tile_hist, int n_tiles,
+                         int32_t* local_rank, int32_t* err) {
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(route_tile_kernel<EPL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    route_tile_kernel<EPL><<<grid, kRouteThreads, smem, s>>>(logits, T, E, P, k, rep_off, rep_ids, topk_e,
+                                                            gates, phys, tile_hist, n_tiles, local_rank,
+                                                            err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
+                        const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys,
+                        int32_t* tile_hist, int32_t* local_rank, int32_t* counts, int32_t* offsets,
+                        int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err,
+                        cudaStream_t s, uint64_t* launches) {
+    const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
+    const size_t items = (size_t)kTileTokens * k;
+    const size_t smem = items * (sizeof(double) + sizeof(float) + 2 * sizeof(int32_t)) +
+                        (size_t)P * sizeof(uint32_t);
+    const int epl = (E + 31) / 32;
+    cudaError_t e;
+    const dim3 grid(n_tiles);
+#define MOE_ROUTE_CASE(N)                                                                          \
+    e = launch_route<N>(grid, smem, s, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, \
+                        tile_hist, n_tiles, local_rank, err)
+    if (epl <= 1) MOE_ROUTE_CASE(1);
+    else if (epl <= 2) MOE_ROUTE_CASE(2);
+    else if (epl <= 4) MOE_ROUTE_CASE(4);
+    else if (epl <= 8) MOE_ROUTE_CASE(8);
+    else if (epl <= 16) MOE_ROUTE_CASE(16);
+    else MOE_ROUTE_CASE(32);
+#undef MOE_ROUTE_CASE
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+
+    column_scan_kernel<<<(P + 7) / 8, kScanThreads, 0, s>>>(tile_hist, n_tiles, P, counts);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    *launches += 1;
+
+    const int n = T * k;
+    assign_kernel<<<(n + kAssignThreads - 1) / kAssignThreads, kAssignThreads, (P + 1) * sizeof(int32_t),
+                    s>>>(phys, tile_hist, n_tiles, local_rank, counts, T, P, k, offsets, slot, src_token,
+                         src_k, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    *launches += 1;
+    return cudaSuccess;
+}
+
+}  // namespace moe

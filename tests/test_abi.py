@@ -1,0 +1,144 @@
+"""Host-only tests of the C ABI (no GPU needed): the library loads, exports
+every function include/moe.h declares, sizes the pool as documented and
+rejects bad arguments before launching anything."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from combine_moe_plan_gb300 import build as moe_build
+from combine_moe_plan_gb300 import moe
+
+
+@pytest.fixture(scope="module")
+def L():
+    moe_build.build()
+    return moe.lib()
+
+
+def _desc(T=64, H=256, E=8, P=8, k=2, group=128, n_sets=2):
+    return moe.Desc(T, H, E, P, k, group, n_sets)
+
+
+def test_exports_every_header_symbol(L):
+    names = moe.header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+    # and nothing but the API is exported under the moe_ prefix
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T moe_" in ln}
+    assert exported == set(names)
+
+
+def test_status_strings(L):
+    for rc in moe.STATUS:
+        assert L.moe_status_str(rc)
+    assert L.moe_status_str(0) == b"ok"
+
+
+def _bytes(L, d):
+    n = ctypes.c_size_t()
+    rc = L.moe_pool_bytes(ctypes.byref(d), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_pool_bytes_layout(L):
+    rc, n = _bytes(L, _desc(T=4096, H=7168, E=256, P=288, k=8))
+    assert rc == 0
+    R, H = 4096 * 8, 7168
+    per_set_payload = R * H + R * 56 * 4 + R * H * 2  # codes + scales + ex_out
+    assert n >= 2 * per_set_payload
+    assert n < 2 * per_set_payload * 1.25  # metadata + staging are small next to the rows
+    rc1, n1 = _bytes(L, _desc(T=4096, H=7168, E=256, P=288, k=8, n_sets=1))
+    assert rc1 == 0 and abs(2 * n1 - n) < 4096
+
+
+@pytest.mark.parametrize("field,val,rc", [
+    ("T_max", 0, -2), ("H", 200, -2), ("H", 64, -2), ("E", 0, -2), ("P", 4, -2), ("k", 0, -2),
+    ("k", 9, -2), ("group", 64, -2), ("n_sets", 0, -2), ("n_sets", 5, -2), ("E", 2000, -2)])
+def test_pool_bytes_rejects(L, field, val, rc):
+    d = _desc()
+    setattr(d, field, val)
+    assert _bytes(L, d)[0] == rc
+
+
+def _fake_pool(L, **kw):
+    d = _desc(**kw)
+    rc, n = _bytes(L, d)
+    assert rc == 0
+    h = ctypes.c_void_p()
+    fake_ws = ctypes.c_void_p(1 << 40)  # 256-aligned address that is never dereferenced on the host
+    assert L.moe_pool_init(ctypes.byref(d), fake_ws, n, ctypes.byref(h)) == 0
+    return h, n
+
+
+def test_pool_init_checks(L):
+    d = _desc()
+    rc, n = _bytes(L, d)
+    h = ctypes.c_void_p()
+    assert L.moe_pool_init(ctypes.byref(d), ctypes.c_void_p(1 << 40), n - 1, ctypes.byref(h)) == -5
+    assert L.moe_pool_init(ctypes.byref(d), ctypes.c_void_p((1 << 40) + 16), n, ctypes.byref(h)) == -3
+    assert L.moe_pool_init(ctypes.byref(d), None, n, ctypes.byref(h)) == -1
+    h, _ = _fake_pool(L)
+    v = moe.View()
+    assert L.moe_pool_view(h, 0, ctypes.byref(v)) == 0
+    assert v.rows == 64 * 2 and v.scale_stride == 4
+    addrs = [getattr(v, f) for f, _ in moe.View._fields_[:12]]
+    assert all(a % 256 == 0 for a in addrs)
+    assert L.moe_pool_view(h, 2, ctypes.byref(v)) == -4
+    assert L.moe_pool_destroy(h) == 0
+
+
+def test_calls_rejected_before_launch(L):
+    h, _ = _fake_pool(L)
+    good = ctypes.c_void_p(1 << 41)
+    odd = ctypes.c_void_p((1 << 41) + 4)
+    # T out of range, bad set, NULL and misaligned pointers
+    assert L.moe_plan(h, good, 0, None, None, 0, None) == -2
+    assert L.moe_plan(h, good, 65, None, None, 0, None) == -2
+    assert L.moe_plan(h, good, 8, None, None, 2, None) == -4
+    assert L.moe_plan(h, None, 8, None, None, 0, None) == -1
+    assert L.moe_plan(h, odd, 8, None, None, 0, None) == -3
+    assert L.moe_plan(h, good, 8, good, None, 0, None) == -1  # half a replica map
+    assert L.moe_plan(None, good, 8, None, None, 0, None) == -1
+    # dispatch / combine before any plan on this set
+    assert L.moe_dispatch(h, good, 8, 0, None) == -9
+    assert L.moe_identity_experts(h, 8, 0, None) == -9
+    assert L.moe_combine(h, None, good, 8, 0, None) == -9
+    assert L.moe_combine(h, None, None, 8, 0, None) == -1
+    assert L.moe_dispatch(h, odd, 8, 0, None) == -3
+    L.moe_pool_destroy(h)
+
+
+def test_replica_map_needed_when_P_exceeds_E(L):
+    h, _ = _fake_pool(L, E=8, P=10)
+    assert L.moe_plan(h, ctypes.c_void_p(1 << 41), 8, None, None, 0, None) == -8
+    L.moe_pool_destroy(h)
+
+
+def test_replica_check(L):
+    def rc(off, ids, E, P):
+        return moe.replica_check(np.array(off), np.array(ids), E, P)
+    assert rc([0, 2, 3], [0, 2, 1], 2, 3) == 0
+    assert rc([0, 1, 2], [1, 0], 2, 2) == 0
+    assert rc([0, 2, 3], [0, 0, 1], 2, 3) == -8    # physical id used twice
+    assert rc([0, 0, 3], [0, 1, 2], 2, 3) == -8    # expert without a replica
+    assert rc([0, 2, 2], [0, 1], 2, 2) == -8
+    assert rc([1, 2, 3], [0, 1, 2], 2, 3) == -8
+    assert rc([0, 2, 3], [0, 3, 1], 2, 3) == -8    # id out of range
+    from combine_moe_plan_gb300 import workloads as wl
+    w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
+    off, ids = wl.make_replica_map(w)
+    assert rc(off, ids, w.E, w.P) == 0
+
+
+def test_binding_has_no_oracle_or_cpu_path():
+    """The product package never imports, loads or runs the oracle."""
+    import pathlib
+    import re
+    pkg = pathlib.Path(moe.__file__).parent
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle)|moe_oracle|libmoe_oracle", re.M)
+    for f in list(pkg.glob("*.py")) + list(pkg.glob("csrc/*")):
+        assert not pat.search(f.read_text()), f

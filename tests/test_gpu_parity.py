@@ -1,0 +1,255 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Bar: bit-exact for top-k experts, physical experts, counts, offsets, slots,
+inverse maps, INT8 codes and fp32 scales; gates within 1 fp32 ulp (fp64
+softmax rounded once on both sides, so in practice identical); combine output
+within 1 bf16 ulp (identical unless a gate differed).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_plan_gb300 import moe
+from combine_moe_plan_gb300 import workloads as wl
+from tests.gpu_util import (Run, assert_y_close, compare_plan, dev, dev_bf16, ensure_built, f32_bits,
+                            host_u16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+# Oracle-sized variants of every workload: several 32-token tiles plus a
+# ragged tail (or the workload's own T where it is already small).
+SMALL = [("t64_h256_e8_k2", 64), ("t96_h7168_e256_k8", 96), ("t4096_h7168_e256p288_k8", 300),
+         ("t16384_h2048_e64_k6", 1000), ("t30720_h7168_e256_k8", 200)]
+
+
+def _check_all(w, inp, run, ex_out=None):
+    ref = oracle.forward(inp["logits"], inp["x"], w.k, inp["rep_off"], inp["rep_ids"], w.P, ex_out=ex_out)
+    compare_plan(run.plan_host(), ref, w.name)
+    R, G = run.T * w.k, w.G
+    np.testing.assert_array_equal(run.v["codes"][:R].cpu().numpy(), ref["codes"], err_msg="codes")
+    np.testing.assert_array_equal(f32_bits(run.v["scales"][:R, :G].cpu().numpy()), f32_bits(ref["scales"]),
+                                  err_msg="scales")
+    if ex_out is None:
+        np.testing.assert_array_equal(host_u16(run.v["ex_out"][:R]), ref["ex_out"], err_msg="identity experts")
+    nd = assert_y_close(host_u16(run.y), ref["y"], w.name)
+    assert run.err == 0
+    return nd
+
+
+@pytest.mark.parametrize("name,T", SMALL)
+def test_small_parity_generated_experts(name, T):
+    w = wl.small_variant(wl.WORKLOADS[name], T)
+    inp = wl.make_inputs(w)
+    ex = inp.get("ex_out")
+    run = Run(w, inp, ex_out=ex)
+    _check_all(w, inp, run, ex_out=ex)
+
+
+@pytest.mark.parametrize("name,T", SMALL)
+def test_small_parity_identity_experts_roundtrip(name, T):
+    w = wl.small_variant(wl.WORKLOADS[name], T)
+    inp = wl.make_inputs(w, with_expert_out=False)
+    run = Run(w, inp)
+    _check_all(w, inp, run)
+    # round trip: y recovers x within the INT8 bound plus two bf16 roundings
+    x = wl.bf16_bits_to_f32(inp["x"]).astype(np.float64)
+    y = wl.bf16_bits_to_f32(host_u16(run.y)).astype(np.float64)
+    _, s = oracle.quantize(inp["x"])
+    scale = np.repeat(s.astype(np.float64), 128, axis=1)
+    bound = scale * (0.5 + 2.0 ** -12) + 2.0 ** -7 * (np.abs(x) + 0.5 * scale) + 127 * scale * 2.0 ** -20
+    assert np.all(np.abs(y - x) <= bound)
+
+
+def test_full_bench_workload_parity():
+    """The bench workload at full size (4096 x 7168, 288 physical experts,
+    top-8), compared in full."""
+    w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
+    inp = wl.make_inputs(w)
+    run = Run(w, inp, ex_out=inp["ex_out"])
+    _check_all(w, inp, run, ex_out=inp["ex_out"])
+    # replicas carry traffic: every physical slot of a hot expert got tokens
+    counts = run.plan_host()["counts"]
+    assert (counts[w.E:] > 0).all()
+
+
+def test_full_16384_ten_iterations_double_buffered():
+    """16384 x 2048, 64 experts, top-6: 10 back-to-back iterations alternating
+    the two buffer sets (buf = i & 1) with no host sync in between; every
+    iteration's output checked against the oracle."""
+    w = wl.WORKLOADS["t16384_h2048_e64_k6"]
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
+    runs = []
+    for i in range(w.iterations):
+        inp = wl.make_inputs(w, seed=i)
+        logits, x, ex = dev(inp["logits"]), dev_bf16(inp["x"]), dev_bf16(inp["ex_out"])
+        buf = i & 1
+        pool.plan(logits, buf=buf)
+        pool.dispatch(x, buf=buf)
+        y = pool.combine(w.T, ex_out=ex, buf=buf)
+        runs.append((inp, y, (logits, x, ex)))
+    assert pool.check() == 0
+    for i, (inp, y, _) in enumerate(runs):
+        pl = oracle.plan(inp["logits"], w.k)
+        y_ref = oracle.combine(inp["ex_out"], pl["slot"], pl["gates"])
+        assert_y_close(host_u16(y), y_ref, f"iteration {i}")
+    # the last two iterations' metadata and dispatch rows are still in the sets
+    for i in (w.iterations - 2, w.iterations - 1):
+        inp = runs[i][0]
+        v = pool.view(i & 1)
+        ref = oracle.plan(inp["logits"], w.k)
+        np.testing.assert_array_equal(v["slot"].cpu().numpy(), ref["slot"])
+        codes, scales = oracle.dispatch(inp["x"], ref["slot"])
+        np.testing.assert_array_equal(v["codes"][:w.rows].cpu().numpy(), codes)
+
+
+def test_full_30720_sampled():
+    """Global decode batch 30720 x 7168, 256 experts, top-8, buffers sized for
+    the worst case: plan metadata compared in full, dispatch rows and combine
+    outputs on a sample of tokens the oracle computes one by one."""
+    w = wl.WORKLOADS["t30720_h7168_e256_k8"]
+    inp = wl.make_inputs(w)
+    run = Run(w, inp, ex_out=inp["ex_out"])
+    ref = oracle.plan(inp["logits"], w.k)
+    compare_plan(run.plan_host(), ref, w.name)
+    rng = np.random.default_rng(0)
+    toks = np.unique(np.concatenate([[0, 1, 31, 32, w.T - 1], rng.choice(w.T, 120, replace=False)]))
+    q, s = oracle.quantize(inp["x"][toks])
+    codes = run.v["codes"]
+    scales = run.v["scales"]
+    for i, t in enumerate(toks):
+        for j in range(w.k):
+            r = int(ref["slot"][t, j])
+            np.testing.assert_array_equal(codes[r].cpu().numpy(), q[i])
+            np.testing.assert_array_equal(f32_bits(scales[r, :w.G].cpu().numpy()), f32_bits(s[i]))
+    y_ref = oracle.combine_tokens(inp["ex_out"], ref["slot"], ref["gates"], toks)
+    assert_y_close(host_u16(run.y)[toks], y_ref, w.name)
+    assert run.err == 0
+
+
+# ------------------------------------------------------------ edge cases --
+
+def _custom(T, H, E, P, k, logits, x=None, rep_off=None, rep_ids=None, seed=0, T_max=None, pool=None):
+    w = wl.Workload("custom", T=T, H=H, E=E, P=P, k=k)
+    rng = np.random.default_rng(seed)
+    if x is None:
+        x = wl.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    inp = {"logits": np.ascontiguousarray(logits, np.float32), "x": x, "rep_off": rep_off, "rep_ids": rep_ids}
+    ex = wl.f32_to_bf16_bits(rng.standard_normal((T * k, H)).astype(np.float32))
+    run = Run(w, inp, ex_out=ex, T_max=T_max, pool=pool)
+    _check_all(w, inp, run, ex_out=ex)
+    run2 = Run(w, inp, T_max=T_max, pool=pool)
+    _check_all(w, inp, run2)
+    return run
+
+
+def test_single_token():
+    _custom(1, 256, 8, 8, 2, np.random.default_rng(1).standard_normal((1, 8)))
+
+
+def test_k_equals_E_and_k1():
+    rng = np.random.default_rng(2)
+    _custom(70, 128, 8, 8, 8, rng.standard_normal((70, 8)))
+    _custom(70, 384, 16, 16, 1, rng.standard_normal((70, 16)))
+
+
+def test_ties_and_signed_zero():
+    rng = np.random.default_rng(3)
+    vals = np.array([-1.0, -0.0, 0.0, 0.5, 0.5, 2.0], np.float32)
+    _custom(97, 256, 40, 40, 5, rng.choice(vals, size=(97, 40)))
+
+
+def test_everyone_on_one_expert():
+    """Worst-case capacity: all tokens pick expert 0 first."""
+    rng = np.random.default_rng(4)
+    lg = rng.standard_normal((300, 64)).astype(np.float32)
+    lg[:, 0] += 100.0
+    run = _custom(300, 512, 64, 64, 4, lg)
+    assert run.plan_host()["counts"][0] == 300
+
+
+def test_max_experts_and_max_k():
+    rng = np.random.default_rng(5)
+    _custom(65, 128, 1024, 1024, 32, rng.standard_normal((65, 1024)))
+
+
+def test_three_replicas_and_zero_groups():
+    """Expert 0 has three physical replicas; some activation groups are all zero."""
+    E, P = 6, 9
+    off = np.array([0, 3, 4, 5, 7, 8, 9], np.int32)   # expert 0: 3 replicas, expert 3: 2
+    ids = np.array([0, 6, 8, 1, 2, 3, 7, 4, 5], np.int32)
+    rng = np.random.default_rng(6)
+    lg = rng.standard_normal((130, E)).astype(np.float32)
+    lg[:, 0] += 3.0
+    x = rng.standard_normal((130, 384)).astype(np.float32)
+    x[5, :] = 0.0
+    x[7, 128:256] = -0.0
+    _custom(130, 384, E, P, 3, lg, x=wl.f32_to_bf16_bits(x), rep_off=off, rep_ids=ids)
+
+
+def test_pool_reuse_smaller_T_and_ragged_tail():
+    """A pool sized for 256 tokens serves a 256-token call, then a 33-token
+    call (one full tile plus one token) on the same set."""
+    rng = np.random.default_rng(7)
+    pool = moe.Pool(256, 256, 32, 32, 4, n_sets=2)
+    _custom(256, 256, 32, 32, 4, rng.standard_normal((256, 32)), pool=pool)
+    _custom(33, 256, 32, 32, 4, rng.standard_normal((33, 32)), pool=pool)
+
+
+def test_outlier_workload_scales():
+    """The decode-batch workload's x50 outliers dominate their groups' scales."""
+    w = wl.WORKLOADS["t96_h7168_e256_k8"]
+    inp = wl.make_inputs(w)
+    run = Run(w, inp, ex_out=inp["ex_out"])
+    s = run.v["scales"][:w.rows, :w.G].cpu().numpy()
+    assert s.max() > 20 * np.median(s)
+
+
+# --------------------------------------------------------- error reporting --
+
+def test_device_error_word_bad_replica_map():
+    """A replica map with an id outside [0, P) is caught by the kernel's own
+    bounds check: the error word says so and nothing is written out of range."""
+    E, P, k, T, H = 4, 6, 2, 40, 128
+    off = dev(np.array([0, 2, 3, 5, 6], np.int32))
+    ids = dev(np.array([0, 4, 1, 2, 99, 3], np.int32))  # 99 is out of range
+    pool = moe.Pool(T, H, E, P, k)
+    logits = dev(np.random.default_rng(8).standard_normal((T, E)).astype(np.float32))
+    x = dev_bf16(wl.f32_to_bf16_bits(np.ones((T, H), np.float32)))
+    pool.plan(logits, off, ids)
+    pool.dispatch(x)
+    pool.combine(T)
+    err = pool.check()
+    assert err & moe.DEVERR_REPLICA
+    assert err & moe.DEVERR_SLOT
+    pool.clear_error()
+    assert pool.check() == 0
+
+
+def test_device_error_word_duplicate_physical_id():
+    E, P, k, T, H = 4, 4, 2, 64, 128
+    off = dev(np.array([0, 1, 2, 3, 4], np.int32))
+    ids = dev(np.array([0, 0, 2, 3], np.int32))  # experts 0 and 1 share a slot
+    pool = moe.Pool(T, H, E, P, k)
+    lg = np.zeros((T, E), np.float32)
+    lg[:, :2] = 5.0  # every token picks experts 0 and 1
+    pool.plan(dev(lg), off, ids)
+    pool.dispatch(dev_bf16(wl.f32_to_bf16_bits(np.ones((T, H), np.float32))))
+    pool.combine(T)
+    assert pool.check() & moe.DEVERR_DUPLICATE
+
+
+def test_launch_count():
+    w = wl.small_variant(wl.WORKLOADS["t64_h256_e8_k2"], 64)
+    inp = wl.make_inputs(w, with_expert_out=False)
+    pool = moe.Pool(64, w.H, w.E, w.P, w.k)
+    n0 = pool.launches()
+    Run(w, inp, pool=pool)
+    # plan = route + column scan + assign; then dispatch, identity experts, combine
+    assert pool.launches() - n0 == 6
