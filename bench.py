@@ -47,6 +47,7 @@ def _args():
     ap.add_argument("--workload", default=wl.BENCH_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
     return ap.parse_args()
 
 
@@ -179,6 +180,33 @@ def run_reference(a, w: wl.Workload):
     }), flush=True)
 
 
+def _e2e(a, w, inp, pool, ex_host, rep_off, rep_ids, ys, stream, ws):
+    """ms per step of moe_step_host from pinned host buffers (copies included)."""
+    import torch
+    import torch.distributed as dist
+    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+    h_x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_ex = ex_host.pin_memory()
+    h_y = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    for i in range(3):
+        pool.step_host(h_logits, h_x, h_y, h_ex, rep_off, rep_ids, buf=i & 1)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    e0.record(stream)
+    for i in range(a.e2e_steps):
+        pool.step_host(h_logits, h_x, h_y, h_ex, rep_off, rep_ids, buf=i & 1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
+    if not torch.equal(h_y, ys[(a.warmup + a.steps - 1) & 1].cpu()):
+        raise RuntimeError("moe_step_host output differs from the device-resident path")
+
+    return e2e_ms
+
+
 def run_ours(a, w: wl.Workload):
     import torch
     import torch.distributed as dist
@@ -264,32 +292,15 @@ def run_ours(a, w: wl.Workload):
     mean_us = {k: 1e3 * statistics.fmean(v) for k, v in per.items()}
 
     # ---- e2e: whole layer from pinned host buffers through moe_step_host ----
-    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
-    h_x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_ex = ex_host.pin_memory()
-    h_y = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-    for i in range(3):
-        pool.step_host(h_logits, h_x, h_y, h_ex, rep_off, rep_ids, buf=i & 1)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        dist.barrier()
-    e0.record(stream)
-    for i in range(a.e2e_steps):
-        pool.step_host(h_logits, h_x, h_y, h_ex, rep_off, rep_ids, buf=i & 1)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
-    if not torch.equal(h_y, ys[(a.warmup + a.steps - 1) & 1].cpu()):
-        raise RuntimeError("moe_step_host output differs from the device-resident path")
+    e2e_ms = float("nan")
+    if not a.no_e2e:
+        e2e_ms = _e2e(a, w, inp, pool, ex_host, rep_off, rep_ids, ys, stream, ws)
 
     # ---- max over ranks ----
     if ws > 1:
         t = torch.tensor([ms, e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, e2e_ms = t.tolist()
-
     if rank == 0:
         bytes_ = w.algorithmic_bytes()
         peak, peak_src = _peaks()
@@ -316,9 +327,10 @@ def run_ours(a, w: wl.Workload):
             "roofline": {"kernel": "combine_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                          "peak_source": peak_src},
-            "e2e": {"value": w.T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": int(inp["logits"].nbytes + inp["x"].nbytes + inp["ex_out"].nbytes),
-                    "d2h_bytes_per_step": int(w.T * w.H * 2), "ms_per_step": e2e_ms},
+            "e2e": None if a.no_e2e else {
+                "value": w.T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(inp["logits"].nbytes + inp["x"].nbytes + inp["ex_out"].nbytes),
+                "d2h_bytes_per_step": int(w.T * w.H * 2), "ms_per_step": e2e_ms},
             "gpu_launches": int(launches),
             "clocks": clocks,
         }
