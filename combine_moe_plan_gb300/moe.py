@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
         "moe_identity_experts": [vp, i32, ctypes.c_int, vp],
         "moe_combine": [vp, vp, vp, i32, ctypes.c_int, vp],
         "moe_step_host": [vp, vp, vp, vp, vp, i32, vp, vp, ctypes.c_int, vp],
+        "moe_plan_static": [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -210,3 +211,26 @@ class Pool:
         n = ctypes.c_uint64()
         _call("moe_pool_launches", self.handle, ctypes.byref(n))
         return n.value
+
+
+def plan_static(logits, k, P=None, rep_off=None, rep_ids=None, out=None, stream=None) -> dict:
+    """moe_plan_static: routing metadata into caller-owned tensors, with no
+    device allocation inside the library (its scratch is a fixed 4 MiB array
+    in the library's device image).  ``out`` may hold preallocated tensors
+    (topk_e, gates, phys, counts, offsets, slot, src_token, src_k,
+    error_word); missing ones are allocated here by torch, outside the call."""
+    T, E = logits.shape
+    P = E if P is None else P
+    dev = logits.device
+    shapes = {"topk_e": ((T, k), torch.int32), "gates": ((T, k), torch.float32), "phys": ((T, k), torch.int32),
+              "counts": ((P,), torch.int32), "offsets": ((P + 1,), torch.int32), "slot": ((T, k), torch.int32),
+              "src_token": ((T * k,), torch.int32), "src_k": ((T * k,), torch.int32),
+              "error_word": ((1,), torch.int32)}
+    out = dict(out or {})
+    for name, (shape, dtype) in shapes.items():
+        if name not in out:
+            out[name] = (torch.zeros if name == "error_word" else torch.empty)(shape, dtype=dtype, device=dev)
+    _call("moe_plan_static", _ptr(logits), T, E, P, k, _ptr(rep_off), _ptr(rep_ids),
+          *[_ptr(out[n]) for n in ("topk_e", "gates", "phys", "counts", "offsets", "slot", "src_token", "src_k",
+                                    "error_word")], _stream(stream))
+    return out

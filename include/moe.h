@@ -214,6 +214,37 @@ MOE_API int moe_step_host(moe_pool* pool, const float* h_logits, const uint16_t*
                           const uint16_t* h_ex_out, uint16_t* h_y, int32_t T,
                           const int32_t* rep_off, const int32_t* rep_ids, int buf, void* stream);
 
+/*
+ * moe_plan_static: moe_plan for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists because some callers
+ * have no allocator to give the pool workspace: code replayed inside a CUDA
+ * graph built elsewhere, plugins whose host framework owns every device
+ * allocation, or processes that must not grow their device footprint after
+ * start-up.
+ *
+ * Computes exactly what moe_plan computes (same kernels), into the caller's
+ * own device arrays instead of a pool set:
+ *   logits [T, E] fp32 in; topk_e, phys, slot int32 [T, k], gates fp32 [T, k],
+ *   counts int32 [P], offsets int32 [P+1], src_token, src_k int32 [T*k] out;
+ *   error_word int32 [1]: device error bits are OR-ed in (zero it first).
+ *   rep_off / rep_ids: device replica map as for moe_plan, or both NULL (P == E).
+ * Its scratch (per-tile expert counts and in-tile ranks) lives in a fixed
+ * 4 MiB array in this library's device image, held on every GPU that loads it
+ * until the process exits.  Sizes whose scratch needs more,
+ * 4 * (P * ceil(T / 32) + T * k) bytes (each part rounded up to 256), return
+ * MOE_ERR_SIZE before anything is launched.  No cudaMalloc or cudaFree is
+ * called.
+ *   - All calls share that array: calls whose kernels overlap on the GPU
+ *     (other streams, other host threads) race and give wrong slots.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make it before any stream capture begins.
+ */
+MOE_API int moe_plan_static(const float* logits, int32_t T, int32_t E, int32_t P, int32_t k,
+                            const int32_t* rep_off, const int32_t* rep_ids, int32_t* topk_e,
+                            float* gates, int32_t* phys, int32_t* counts, int32_t* offsets,
+                            int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* error_word,
+                            void* stream);
+
 /* Static string for a moe_status value. */
 MOE_API const char* moe_status_str(int status);
 
