@@ -9,9 +9,9 @@
 // fp32 with one fused multiply-add per copy, in ascending j, so the result
 // does not depend on scheduling.
 //
-// GPU mapping: one warp per (token, 512-element segment); a lane owns two
-// 8-element chunks (16 bytes each) and keeps up to 8 copies x 2 chunks of
-// 16-byte loads in flight before it accumulates them in order.
+// GPU mapping: one warp per (token, 256-element segment); a lane owns one
+// 8-element chunk (16 bytes) of every copy and keeps up to 8 copies' 16-byte
+// loads in flight before it accumulates them in order.
 #include "moe_internal.h"
 #include "ptx.cuh"
 
@@ -19,7 +19,7 @@ namespace moe {
 namespace {
 
 constexpr int kCombineThreads = 256;  // 8 warps
-constexpr int kChunks = 2;            // 16-byte chunks per lane per item
+constexpr int kChunks = 1;            // 16-byte chunks per lane per item
 constexpr int kSegElems = 32 * 8 * kChunks;
 constexpr int kBatch = 8;             // copies loaded before accumulating
 
@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ slot,
                const float* __restrict__ gates, int T, int H, int k, uint16_t* __restrict__ y,
                int32_t* __restrict__ err) {
+    grid_dependency_sync();
+    allow_dependents();
     const int lane = threadIdx.x & 31;
     const int segs = (H + kSegElems - 1) / kSegElems;
     const long long item = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
@@ -110,8 +112,8 @@ cudaError_t launch_combine(const uint16_t* ex_out, const int32_t* slot, const fl
                            uint16_t* y, int32_t* err, cudaStream_t s, uint64_t* launches) {
     const long long items = (long long)T * ((H + kSegElems - 1) / kSegElems);
     const long long blocks = (items + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
-    combine_kernel<<<(unsigned)blocks, kCombineThreads, 0, s>>>(ex_out, slot, gates, T, H, k, y, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineThreads), 0, s, ex_out, slot,
+                               gates, T, H, k, y, err);
     if (e == cudaSuccess) *launches += 1;
     return e;
 }

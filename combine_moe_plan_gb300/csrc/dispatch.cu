@@ -36,6 +36,8 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
 __global__ void __launch_bounds__(kDispatchThreads)
 dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ slot,
                 int8_t* __restrict__ codes, float* __restrict__ scales, int Gs, int32_t* __restrict__ err) {
+    grid_dependency_sync();
+    allow_dependents();
     const int lane = threadIdx.x & 31;
     const int segs = (H + kSegElems - 1) / kSegElems;
     const long long item = (long long)blockIdx.x * (kDispatchThreads / 32) + (threadIdx.x >> 5);
@@ -101,6 +103,8 @@ constexpr int kExpertThreads = 256;
 __global__ void __launch_bounds__(kExpertThreads)
 identity_experts_kernel(const int8_t* __restrict__ codes, const float* __restrict__ scales, int rows, int H,
                         int Gs, uint16_t* __restrict__ ex_out) {
+    grid_dependency_sync();
+    allow_dependents();
     const int per_row = H / 16;
     const long long n = (long long)rows * per_row;
     for (long long c = (long long)blockIdx.x * kExpertThreads + threadIdx.x; c < n;
@@ -132,8 +136,8 @@ cudaError_t launch_dispatch(const uint16_t* x, int T, int H, int k, const int32_
                             float* scales, int Gs, int32_t* err, cudaStream_t s, uint64_t* launches) {
     const long long items = (long long)T * ((H + kSegElems - 1) / kSegElems);
     const long long blocks = (items + (kDispatchThreads / 32) - 1) / (kDispatchThreads / 32);
-    dispatch_kernel<<<(unsigned)blocks, kDispatchThreads, 0, s>>>(x, T, H, k, slot, codes, scales, Gs, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(dispatch_kernel, dim3((unsigned)blocks), dim3(kDispatchThreads), 0, s, x, T, H, k,
+                               slot, codes, scales, Gs, err);
     if (e == cudaSuccess) *launches += 1;
     return e;
 }
@@ -144,8 +148,8 @@ cudaError_t launch_identity_experts(const int8_t* codes, const float* scales, in
     long long blocks = (n + kExpertThreads - 1) / kExpertThreads;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    identity_experts_kernel<<<(unsigned)blocks, kExpertThreads, 0, s>>>(codes, scales, rows, H, Gs, ex_out);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(identity_experts_kernel, dim3((unsigned)blocks), dim3(kExpertThreads), 0, s, codes,
+                               scales, rows, H, Gs, ex_out);
     if (e == cudaSuccess) *launches += 1;
     return e;
 }

@@ -34,6 +34,25 @@ struct Geometry {
 
 int make_geometry(const moe_desc* d, Geometry* g);
 
+// Launch with programmatic stream serialization, so that the kernel can be
+// scheduled while the previous kernel in the stream drains (the kernel itself
+// waits for it in grid_dependency_sync before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Launchers: enqueue on `s`, return cudaGetLastError() after the launch(es).
 // Each adds the number of kernels it launched to *launches.
 cudaError_t launch_plan(const float* logits, int T, int E, int P, int k,

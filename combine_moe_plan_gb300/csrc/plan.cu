@@ -8,10 +8,10 @@
 // section 3.5: token placement -> expert-window aggregation.
 //
 // Three launches:
-//   route_tile   one CTA per tile of 32 tokens.  A warp finds a token's top-k
-//                with k rounds of shuffle arg-max (ties -> lower expert id),
-//                then the CTA computes gates in fp64 (batched over the
-//                tile's (token, j) pairs), applies the replica map, and sets
+//   route_tile   one CTA of 32 warps per tile of 32 tokens, one warp per
+//                token: k rounds of shuffle arg-max (ties -> lower expert
+//                id).  The CTA then computes the gates in fp64 with one
+//                (token, j) pair per thread, applies the replica map, and sets
 //                bit t of a shared-memory mask per physical expert.  From the
 //                mask: the tile's count per expert (popc) and each copy's rank
 //                among earlier tokens of the tile (popc of the lower bits).
@@ -32,8 +32,16 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteThreads = 256;                 // 8 warps
-constexpr int kTokensPerWarp = kTileTokens / 8;    // 4
+constexpr int kRouteThreads = 32 * kTileTokens;  // one warp per token of the tile
+
+// Monotone map of finite floats onto uint32 (a < b  <=>  key(a) < key(b));
+// -0 is folded onto +0 first, so equal values give equal keys.  Every finite
+// value maps above 0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t b = __float_as_uint(f);
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
 
 template <int EPL>  // logits per lane = ceil(E / 32)
 __global__ void __launch_bounds__(kRouteThreads)
@@ -43,98 +51,109 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
                   int32_t* __restrict__ phys, int32_t* __restrict__ tile_hist, int n_tiles,
                   int32_t* __restrict__ local_rank, int32_t* __restrict__ err) {
     extern __shared__ __align__(16) unsigned char smem[];
-    double* e64 = reinterpret_cast<double*>(smem);                       // [32*k]
-    float* sel_v = reinterpret_cast<float*>(e64 + kTileTokens * k);      // [32*k]
-    int32_t* sel_e = reinterpret_cast<int32_t*>(sel_v + kTileTokens * k); // [32*k]
-    int32_t* sel_p = sel_e + kTileTokens * k;                            // [32*k]
-    uint32_t* mask = reinterpret_cast<uint32_t*>(sel_p + kTileTokens * k); // [P]
+    double* e64 = reinterpret_cast<double*>(smem);                          // [32*k]
+    double* rsum = e64 + kTileTokens * k;                                   // [32] 1 / sum per token
+    float* sel_v = reinterpret_cast<float*>(rsum + kTileTokens);            // [32*k]
+    int32_t* sel_e = reinterpret_cast<int32_t*>(sel_v + kTileTokens * k);  // [32*k]
+    int32_t* sel_p = sel_e + kTileTokens * k;                               // [32*k]
+    uint32_t* mask = reinterpret_cast<uint32_t*>(sel_p + kTileTokens * k);  // [P]
+    int32_t* s_off = reinterpret_cast<int32_t*>(mask + P);                 // [E+1] replica CSR
+    int32_t* s_ids = s_off + (E + 1);                                       // [P]
 
+    grid_dependency_sync();
+    allow_dependents();
     const int tile = blockIdx.x;
-    const int warp = threadIdx.x >> 5;
+    const int tl = threadIdx.x >> 5;  // this warp's token within the tile
     const int lane = threadIdx.x & 31;
     const int t0 = tile * kTileTokens;
+    const int t = t0 + tl;
 
     for (int p = threadIdx.x; p < P; p += kRouteThreads) mask[p] = 0u;
+    if (rep_off != nullptr) {
+        for (int i = threadIdx.x; i <= E; i += kRouteThreads) s_off[i] = rep_off[i];
+        for (int i = threadIdx.x; i < P; i += kRouteThreads) s_ids[i] = rep_ids[i];
+    }
 
-    // ---- top-k: one warp per token ----
-    for (int i = 0; i < kTokensPerWarp; ++i) {
-        const int tl = warp * kTokensPerWarp + i;
-        const int t = t0 + tl;
-        if (t >= T) break;
+    // ---- top-k of token t: k rounds of warp arg-max, ties -> lower id ----
+    // Logits become order-preserving unsigned keys (-0 folded onto +0 so that
+    // equal floats give equal keys); a round is a per-lane max, one warp
+    // max-reduction of the key and one min-reduction of the expert id among
+    // the lanes holding that key.  Key 0 sits below every finite logit and
+    // marks padding and experts already taken.
+    if (t < T) {
         const float* row = logits + (size_t)t * E;
-        float v[EPL];
+        uint32_t key[EPL];
 #pragma unroll
         for (int r = 0; r < EPL; ++r) {
             const int e = r * 32 + lane;
-            v[r] = (e < E) ? __ldg(row + e) : -INFINITY;
+            key[r] = (e < E) ? order_key(__ldg(row + e)) : 0u;
         }
-        uint32_t taken = 0u;
+        int my_e = 0;
         for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int bi = INT_MAX;
+            uint32_t lm = 0u;
+            int li = INT_MAX;
 #pragma unroll
             for (int r = 0; r < EPL; ++r) {
-                const int e = r * 32 + lane;
-                const bool ok = (e < E) && !((taken >> r) & 1u);
-                if (ok && (v[r] > bv || (v[r] == bv && e < bi))) {
-                    bv = v[r];
-                    bi = e;
+                if (key[r] > lm) {  // strict: the lowest r (lowest id) wins a tie
+                    lm = key[r];
+                    li = r * 32 + lane;
                 }
             }
+            const uint32_t m = __reduce_max_sync(kFull, lm);
+            int win = (int)__reduce_min_sync(kFull, (lm == m) ? (uint32_t)li : (uint32_t)INT_MAX);
+            if (win >= E) win = 0;  // only reachable with NaN logits (outside the domain)
+            if (lane == (win & 31)) {
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(kFull, bv, off);
-                const int oi = __shfl_xor_sync(kFull, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
+                for (int r = 0; r < EPL; ++r)
+                    if (r == (win >> 5)) key[r] = 0u;
             }
-            if (bi >= E) bi = 0;  // only reachable with NaN logits (outside the domain)
-            if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
-            if (lane == 0) {
-                sel_v[tl * k + j] = bv;
-                sel_e[tl * k + j] = bi;
-            }
+            if (lane == j) my_e = win;
+        }
+        if (lane < k) {
+            sel_v[tl * k + lane] = __ldg(row + my_e);
+            sel_e[tl * k + lane] = my_e;
         }
     }
     __syncthreads();
 
-    // ---- gates (fp64, rounded once), replica pick, mask ----
+    // ---- gates in fp64: e_j = exp(l_j - l_0) (e_0 = 1 exactly), s = sum over
+    // j ascending, gate = (float)(e_j / s) computed as e_j * (1 / s) ----
     const int n_items = kTileTokens * k;
-    for (int it = threadIdx.x; it < n_items; it += kRouteThreads) {
-        const int tl = it / k;
-        if (t0 + tl < T) e64[it] = exp((double)sel_v[it] - (double)sel_v[tl * k]);
+    const int it = threadIdx.x;  // k <= 32: one (token, j) item per thread
+    const int itl = it / k;
+    const int ij = it - itl * k;
+    const bool item_ok = it < n_items && t0 + itl < T;
+    if (item_ok) e64[it] = (ij == 0) ? 1.0 : exp((double)sel_v[it] - (double)sel_v[itl * k]);
+    __syncthreads();
+    if (threadIdx.x < kTileTokens && t0 + (int)threadIdx.x < T) {
+        double s = 0.0;
+        for (int jj = 0; jj < k; ++jj) s += e64[threadIdx.x * k + jj];
+        rsum[threadIdx.x] = 1.0 / s;
     }
     __syncthreads();
-    for (int it = threadIdx.x; it < n_items; it += kRouteThreads) {
-        const int tl = it / k;
-        const int j = it - tl * k;
-        const int t = t0 + tl;
-        if (t >= T) continue;
-        double s = 0.0;
-        for (int jj = 0; jj < k; ++jj) s += e64[tl * k + jj];
-        const float g = (float)(e64[it] / s);
+    if (item_ok) {
+        const int tt = t0 + itl;
+        const float g = (float)(e64[it] * rsum[itl]);
         const int e = sel_e[it];
         int p = e;
         if (rep_off != nullptr) {
-            const int lo = rep_off[e];
-            const int n = rep_off[e + 1] - lo;
+            const int lo = s_off[e];
+            const int n = s_off[e + 1] - lo;
             if (n < 1 || lo < 0 || lo + n > P) {
                 p = -1;
             } else {
-                p = rep_ids[lo + t % n];
+                p = s_ids[lo + tt % n];
                 if (p < 0 || p >= P) p = -1;
             }
             if (p < 0) set_error(err, MOE_DEVERR_REPLICA);
         }
-        const size_t o = (size_t)t * k + j;
+        const size_t o = (size_t)tt * k + ij;
         topk_e[o] = e;
         gates[o] = g;
         phys[o] = p;
         sel_p[it] = p;
         if (p >= 0) {
-            const uint32_t bit = 1u << tl;
+            const uint32_t bit = 1u << itl;
             const uint32_t old = atomicOr(&mask[p], bit);
             if (old & bit) set_error(err, MOE_DEVERR_DUPLICATE);
         }
@@ -144,13 +163,9 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     // ---- tile histogram (expert-major) and in-tile ranks ----
     for (int p = threadIdx.x; p < P; p += kRouteThreads)
         tile_hist[(size_t)p * n_tiles + tile] = __popc(mask[p]);
-    for (int it = threadIdx.x; it < n_items; it += kRouteThreads) {
-        const int tl = it / k;
-        const int t = t0 + tl;
-        if (t >= T) continue;
+    if (item_ok) {
         const int p = sel_p[it];
-        local_rank[(size_t)t * k + (it - tl * k)] =
-            (p >= 0) ? __popc(mask[p] & ((1u << tl) - 1u)) : 0;
+        local_rank[(size_t)(t0 + itl) * k + ij] = (p >= 0) ? __popc(mask[p] & ((1u << itl) - 1u)) : 0;
     }
 }
 
@@ -161,6 +176,8 @@ constexpr int kScanBatch = 8;  // chunks of 32 tiles loaded before scanning
 
 __global__ void __launch_bounds__(kScanThreads)
 column_scan_kernel(int32_t* __restrict__ tile_hist, int n_tiles, int P, int32_t* __restrict__ counts) {
+    grid_dependency_sync();
+    allow_dependents();
     const int p = blockIdx.x * (kScanThreads / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (p >= P) return;
@@ -228,17 +245,25 @@ assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile
               int k, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
               int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err) {
     extern __shared__ int32_t offs[];  // [P+1]
-    block_offsets<kAssignThreads>(counts, P, offs);
-    if (blockIdx.x == 0)
-        for (int p = threadIdx.x; p <= P; p += kAssignThreads) offsets[p] = offs[p];
+    grid_dependency_sync();
+    allow_dependents();
     const int n = T * k;
     const int it = blockIdx.x * kAssignThreads + threadIdx.x;
+    // Loads that do not depend on the offsets go out before the block scan.
+    int p = -1, base = 0, rank = 0;
+    if (it < n) {
+        p = phys[it];
+        rank = local_rank[it];
+        if (p >= 0 && p < P) base = tile_hist[(size_t)p * n_tiles + (it / k) / kTileTokens];
+    }
+    block_offsets<kAssignThreads>(counts, P, offs);
+    if (blockIdx.x == 0)
+        for (int q = threadIdx.x; q <= P; q += kAssignThreads) offsets[q] = offs[q];
     if (it >= n) return;
     const int t = it / k;
     const int j = it - t * k;
-    const int p = phys[it];
     int r = -1;
-    if (p >= 0 && p < P) r = offs[p] + tile_hist[(size_t)p * n_tiles + t / kTileTokens] + local_rank[it];
+    if (p >= 0 && p < P) r = offs[p] + base + rank;
     if (r < 0 || r >= n) {
         set_error(err, MOE_DEVERR_SLOT);
         slot[it] = -1;
@@ -259,10 +284,8 @@ cudaError_t launch_route(dim3 grid, size_t smem, cudaStream_t s, const float* lo
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    route_tile_kernel<EPL><<<grid, kRouteThreads, smem, s>>>(logits, T, E, P, k, rep_off, rep_ids, topk_e,
-                                                            gates, phys, tile_hist, n_tiles, local_rank,
-                                                            err);
-    return cudaGetLastError();
+    return launch_pdl(route_tile_kernel<EPL>, grid, dim3(kRouteThreads), smem, s, logits, T, E, P, k, rep_off,
+                      rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, err);
 }
 
 }  // namespace
@@ -275,7 +298,8 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
     const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
     const size_t items = (size_t)kTileTokens * k;
     const size_t smem = items * (sizeof(double) + sizeof(float) + 2 * sizeof(int32_t)) +
-                        (size_t)P * sizeof(uint32_t);
+                        kTileTokens * sizeof(double) + (size_t)P * sizeof(uint32_t) +
+                        (size_t)(E + 1 + P) * sizeof(int32_t);
     const int epl = (E + 31) / 32;
     cudaError_t e;
     const dim3 grid(n_tiles);
@@ -292,15 +316,16 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
     if (e != cudaSuccess) return e;
     *launches += 1;
 
-    column_scan_kernel<<<(P + 7) / 8, kScanThreads, 0, s>>>(tile_hist, n_tiles, P, counts);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(column_scan_kernel, dim3((P + 7) / 8), dim3(kScanThreads), 0, s, tile_hist, n_tiles, P, counts);
+    if (e != cudaSuccess) return e;
     *launches += 1;
 
     const int n = T * k;
-    assign_kernel<<<(n + kAssignThreads - 1) / kAssignThreads, kAssignThreads, (P + 1) * sizeof(int32_t),
-                    s>>>(phys, tile_hist, n_tiles, local_rank, counts, T, P, k, offsets, slot, src_token,
-                         src_k, err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(assign_kernel, dim3((n + kAssignThreads - 1) / kAssignThreads), dim3(kAssignThreads),
+                   (P + 1) * sizeof(int32_t), s, phys, (const int32_t*)tile_hist, n_tiles,
+                   (const int32_t*)local_rank, (const int32_t*)counts, T, P, k, offsets, slot, src_token, src_k,
+                   err);
+    if (e != cudaSuccess) return e;
     *launches += 1;
     return cudaSuccess;
 }

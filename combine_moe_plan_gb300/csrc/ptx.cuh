@@ -45,4 +45,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 __device__ __forceinline__ void set_error(int32_t* err, int bits) { atomicOr(err, bits); }
 
+// Programmatic dependent launch.  Every kernel of the library calls
+// grid_dependency_sync() before its first global-memory access: it returns once
+// the preceding kernel in the stream has completed and its writes are visible
+// (immediately if there is none).  allow_dependents() then lets the next
+// kernel's CTAs be scheduled while this grid drains; they park in their own
+// grid_dependency_sync(), so ordering is unchanged -- only launch latency is
+// hidden.
+__device__ __forceinline__ void grid_dependency_sync() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace moe
