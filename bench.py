@@ -121,6 +121,18 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(vals, device=None):
+    """Element-wise max of per-rank timings (ms) over all ranks; identity
+    when not distributed.  The reported time of a multi-rank run is the
+    slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def _oracle_step_fn(w: wl.Workload, inp: dict):
     """A function running the oracle over tokens [a, b) of the workload."""
     import oracle
@@ -297,10 +309,7 @@ def run_ours(a, w: wl.Workload):
         e2e_ms = _e2e(a, w, inp, pool, ex_host, rep_off, rep_ids, ys, stream, ws)
 
     # ---- max over ranks ----
-    if ws > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = t.tolist()
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev)
     if rank == 0:
         bytes_ = w.algorithmic_bytes()
         peak, peak_src = _peaks()

@@ -1,0 +1,72 @@
+"""Host-side multi-rank logic of bench.py, on CPU with the gloo backend
+(world size 2): the reported time is the max over ranks, each rank runs its
+own replica (its own seed), and the reference arm prints on rank 0 only."""
+import json
+import multiprocessing as mp
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(ws),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    import bench
+    from combine_moe_plan_gb300 import workloads as wl
+    out = bench.max_over_ranks([1.0 + rank, 5.0 - rank])
+    w = wl.WORKLOADS["t64_h256_e8_k2"]
+    x0 = wl.make_x(w, seed=rank)[0, :4].tolist()  # each rank draws its own batch
+    dist.barrier()
+    q.put((rank, out, bench._dist(), x0))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, out, d, _ in res:
+        assert out == [2.0, 5.0]
+        assert d == (2, rank, rank)
+    assert res[0][3] != res[1][3]
+
+
+def _ref(env_extra, *args):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                           "--workload", "t64_h256_e8_k2", "--steps", "2", "--warmup", "1", *args],
+                          capture_output=True, text=True, env=env, timeout=300)
+
+
+def test_reference_arm_rank0_only():
+    r1 = _ref({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    r0 = _ref({"RANK": "0", "WORLD_SIZE": "1", "LOCAL_RANK": "0"})
+    assert r0.returncode == 0, r0.stderr
+    lines = [ln for ln in r0.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "t64_h256_e8_k2"
