@@ -5,12 +5,18 @@ gates, replica map, histogram, scan, slots) -> moe_dispatch (INT8 quantize +
 scatter into k expert slots) -> moe_combine (gate-weighted gather-reduce),
 at 4096 tokens x hidden 7168, 256 experts + 32 redundant replicas (288
 physical), top-8.  Expert outputs are synthetic bf16 rows resident in the
-pool's combine buffers.  Consecutive steps alternate the two buffer sets.
+pool's combine buffers.  Step i uses buffer set i mod 2.
 
-Prints ONE JSON line (rank 0).  `value` is tokens/s with inputs already in
-HBM; `e2e` is the same metric through moe_step_host with pinned host buffers
-(host->device copies of logits, x and expert outputs, device->host copy of y
-inside the timed region).
+Phases:
+  A  300 steps serialized on one stream with CUDA events around every call:
+     per-call latencies and the dominant kernel's roofline.
+  B  the K timed steps (the JSON `value`): the two buffer sets on two streams,
+     so step i+1's plan overlaps step i's bandwidth-bound kernels.
+  C  e2e: moe_step_host from pinned host buffers -- logits and x copied in,
+     plan, dispatch, identity experts (the device stand-in for the expert
+     FFNs), combine, y copied out -- also on the two sets/streams.
+
+Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -41,11 +47,11 @@ FALLBACK_HBM_GBS = 6800.0
 def _args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=6000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=wl.BENCH_WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
     return ap.parse_args()
@@ -144,7 +150,7 @@ def _oracle_step_fn(w: wl.Workload, inp: dict):
     return run
 
 
-def cpu_baseline(w: wl.Workload, inp: dict, budget_s: float = 12.0) -> dict:
+def cpu_baseline(w: wl.Workload, inp: dict, budget_s: float = 15.0) -> dict:
     """The oracle as it stands on one host core, on a bounded sample of the
     workload: whole batches while they fit the budget, else a token prefix."""
     run = _oracle_step_fn(w, inp)
@@ -152,8 +158,7 @@ def cpu_baseline(w: wl.Workload, inp: dict, budget_s: float = 12.0) -> dict:
     run(0, min(w.T, 64))
     per_tok = (time.perf_counter() - t0) / min(w.T, 64)
     n_tok = int(max(64, min(w.T, budget_s / max(per_tok, 1e-9))))
-    reps = max(1, int(budget_s / (per_tok * n_tok)))
-    reps = min(reps, 3)
+    reps = max(1, min(30, int(budget_s / (per_tok * n_tok))))
     t0 = time.perf_counter()
     for _ in range(reps):
         run(0, n_tok)
@@ -192,31 +197,29 @@ def run_reference(a, w: wl.Workload):
     }), flush=True)
 
 
-def _e2e(a, w, inp, pool, ex_host, rep_off, rep_ids, ys, stream, ws):
-    """ms per step of moe_step_host from pinned host buffers (copies included)."""
-    import torch
-    import torch.distributed as dist
-    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
-    h_x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_ex = ex_host.pin_memory()
-    h_y = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-    for i in range(3):
-        pool.step_host(h_logits, h_x, h_y, h_ex, rep_off, rep_ids, buf=i & 1)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        dist.barrier()
-    e0.record(stream)
-    for i in range(a.e2e_steps):
-        pool.step_host(h_logits, h_x, h_y, h_ex, rep_off, rep_ids, buf=i & 1)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
-    if not torch.equal(h_y, ys[(a.warmup + a.steps - 1) & 1].cpu()):
-        raise RuntimeError("moe_step_host output differs from the device-resident path")
+class _Streams:
+    """Two streams, one per buffer set: step i runs on stream i & 1, so the
+    latency-bound plan of step i+1 overlaps the bandwidth-bound kernels of
+    step i (the micro-batch overlap the double-buffered pool exists for).
+    Each stream only ever touches its own set, so stream order alone keeps
+    every set's plan -> dispatch -> combine -> next plan sequence intact."""
 
-    return e2e_ms
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.s = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+        self.main = torch.cuda.current_stream()
+
+    def fork(self):
+        e = self.torch.cuda.Event()
+        e.record(self.main)
+        for s in self.s:
+            s.wait_event(e)
+
+    def join(self):
+        for s in self.s:
+            e = self.torch.cuda.Event()
+            e.record(s)
+            self.main.wait_event(e)
 
 
 def run_ours(a, w: wl.Workload):
@@ -238,38 +241,57 @@ def run_ours(a, w: wl.Workload):
     dev = torch.device("cuda", local)
     logits = torch.from_numpy(inp["logits"]).to(dev)
     x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
-    ex_host = torch.from_numpy(inp["ex_out"].view(np.int16)).view(torch.bfloat16)
+    ex_dev = torch.from_numpy(inp["ex_out"].view(np.int16)).view(torch.bfloat16).to(dev)
     rep_off = None if inp["rep_off"] is None else torch.from_numpy(inp["rep_off"]).to(dev)
     rep_ids = None if inp["rep_ids"] is None else torch.from_numpy(inp["rep_ids"]).to(dev)
     pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2, device=dev)
     for b in range(2):
-        pool.view(b)["ex_out"][: w.rows].copy_(ex_host.to(dev))
+        pool.view(b)["ex_out"][: w.rows].copy_(ex_dev)
+    del ex_dev
     ys = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    stream = torch.cuda.current_stream()
+    st = _Streams(torch, dev)
 
-    def step(i, ev=None):
+    def step(i, stream, ev=None):
         b = i & 1
         if ev is not None:
             ev[0].record(stream)
-        pool.plan(logits, rep_off, rep_ids, buf=b)
+        pool.plan(logits, rep_off, rep_ids, buf=b, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        pool.dispatch(x, buf=b)
+        pool.dispatch(x, buf=b, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        pool.combine(w.T, y=ys[b], buf=b)
+        pool.combine(w.T, y=ys[b], buf=b, stream=stream)
         if ev is not None:
             ev[3].record(stream)
 
-    for i in range(a.warmup):
-        step(i)
+    def pipelined(n, i0=0):
+        st.fork()
+        for i in range(i0, i0 + n):
+            step(i, st.s[i & 1])
+        st.join()
+
+    pipelined(a.warmup)
     torch.cuda.synchronize()
     if pool.check() != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    # ---- device-resident timed region ----
-    n_ev = min(a.steps, 400)  # per-kernel events on a subset of steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    # ---- phase A: serialized steps on one stream, per-kernel CUDA events ----
+    n_lat = min(a.steps, 300)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_lat)]
+    for i in range(n_lat):
+        step(i, st.main, evs[i])
+    torch.cuda.synchronize()
+    per = {"plan": [], "dispatch": [], "combine": [], "step": []}
+    for e in evs:
+        per["plan"].append(e[0].elapsed_time(e[1]))
+        per["dispatch"].append(e[1].elapsed_time(e[2]))
+        per["combine"].append(e[2].elapsed_time(e[3]))
+        per["step"].append(e[0].elapsed_time(e[3]))
+    per_us = {k: 1e3 * statistics.median(v) for k, v in per.items()}
+    mean_us = {k: 1e3 * statistics.fmean(v) for k, v in per.items()}
+
+    # ---- phase B (timed region): K steps, the two buffer sets on two streams ----
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
@@ -278,14 +300,9 @@ def run_ours(a, w: wl.Workload):
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = pool.launches()
-    t_start.record(stream)
-    ev_stride = max(1, a.steps // n_ev)
-    k_ev = 0
-    for i in range(a.steps):
-        use = (i % ev_stride == 0) and k_ev < n_ev
-        step(a.warmup + i, evs[k_ev] if use else None)
-        k_ev += int(use)
-    t_end.record(stream)
+    t_start.record(st.main)
+    pipelined(a.steps, a.warmup)
+    t_end.record(st.main)
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
@@ -295,26 +312,18 @@ def run_ours(a, w: wl.Workload):
     err = pool.check()
     if err != 0:
         raise RuntimeError(f"device error word {err:#x}")
-    per = {"plan": [], "dispatch": [], "combine": []}
-    for e in evs[:k_ev]:
-        per["plan"].append(e[0].elapsed_time(e[1]))
-        per["dispatch"].append(e[1].elapsed_time(e[2]))
-        per["combine"].append(e[2].elapsed_time(e[3]))
-    per_us = {k: 1e3 * statistics.median(v) for k, v in per.items()}
-    mean_us = {k: 1e3 * statistics.fmean(v) for k, v in per.items()}
 
-    # ---- e2e: whole layer from pinned host buffers through moe_step_host ----
+    # ---- phase C: e2e through moe_step_host from pinned host buffers ----
     e2e_ms = float("nan")
     if not a.no_e2e:
-        e2e_ms = _e2e(a, w, inp, pool, ex_host, rep_off, rep_ids, ys, stream, ws)
+        e2e_ms = _e2e(a, w, inp, pool, rep_off, rep_ids, st, ws)
 
     # ---- max over ranks ----
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev)
     if rank == 0:
         bytes_ = w.algorithmic_bytes()
         peak, peak_src = _peaks()
-        comb_s = mean_us["combine"] * 1e-6
-        achieved = bytes_["combine"] / comb_s / 1e9
+        achieved = bytes_["combine"] / (mean_us["combine"] * 1e-6) / 1e9
         traffic = _traffic("combine.cu", "combine_kernel")
         tokens = w.T * ws
         out = {
@@ -325,10 +334,13 @@ def run_ours(a, w: wl.Workload):
             "data": "synthetic (seeded; N(0,1) logits + Zipf(1.2) expert bias, N(0,1) bf16 x and expert outputs)",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "P": w.P, "k": w.k,
                        "group": w.group, "parallelism": f"replicas x{ws}",
+                       "schedule": "two buffer sets on two streams (step i on set/stream i mod 2)",
                        "l2": "inputs larger than L2 (about 0.83 GB touched per step, two buffer sets alternate)"},
             "us_per_call": {"plan": per_us["plan"], "dispatch": per_us["dispatch"],
-                            "combine": per_us["combine"], "step": ms * 1e3},
+                            "combine": per_us["combine"], "step_serialized": per_us["step"],
+                            "step_pipelined": ms * 1e3},
             "hbm_gbs": {"step": bytes_["total"] / (ms * 1e-3) / 1e9,
+                        "step_serialized": bytes_["total"] / (per_us["step"] * 1e-6) / 1e9,
                         "dispatch": bytes_["dispatch"] / (per_us["dispatch"] * 1e-6) / 1e9,
                         "combine": bytes_["combine"] / (per_us["combine"] * 1e-6) / 1e9,
                         "step_frac_of_peak": bytes_["total"] / (ms * 1e-3) / 1e9 / peak},
@@ -338,8 +350,10 @@ def run_ours(a, w: wl.Workload):
                          "peak_source": peak_src},
             "e2e": None if a.no_e2e else {
                 "value": w.T * ws / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(inp["logits"].nbytes + inp["x"].nbytes + inp["ex_out"].nbytes),
-                "d2h_bytes_per_step": int(w.T * w.H * 2), "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": int(inp["logits"].nbytes + inp["x"].nbytes),
+                "d2h_bytes_per_step": int(w.T * w.H * 2), "ms_per_step": e2e_ms,
+                "path": "moe_step_host: logits+x host->device, plan, dispatch, identity experts (device "
+                        "stand-in for the expert FFNs), combine, y device->host; two sets on two streams"},
             "gpu_launches": int(launches),
             "clocks": clocks,
         }
@@ -349,6 +363,45 @@ def run_ours(a, w: wl.Workload):
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def _e2e(a, w, inp, pool, rep_off, rep_ids, st, ws):
+    """ms per step of moe_step_host from pinned host buffers (copies inside)."""
+    import torch
+    import torch.distributed as dist
+    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+    h_x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_y = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+
+    def run(n):
+        st.fork()
+        for i in range(n):
+            pool.step_host(h_logits, h_x, h_y[i & 1], None, rep_off, rep_ids, buf=i & 1, stream=st.s[i & 1])
+        st.join()
+
+    run(4)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    e0.record(st.main)
+    run(a.e2e_steps)
+    e1.record(st.main)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
+    # the same layer run from device-resident inputs must give the same y
+    x = h_x.to(pool.workspace.device)
+    pool.plan(h_logits.to(pool.workspace.device), rep_off, rep_ids, buf=0)
+    pool.dispatch(x, buf=0)
+    pool.identity_experts(w.T, buf=0)
+    y = pool.combine(w.T, buf=0)
+    torch.cuda.synchronize()
+    if not (torch.equal(h_y[0], y.cpu()) and torch.equal(h_y[1], y.cpu())):
+        raise RuntimeError("moe_step_host output differs from the device-resident path")
+    if pool.check() != 0:
+        raise RuntimeError("device error word set in the e2e pass")
+    return e2e_ms
 
 
 def main():
