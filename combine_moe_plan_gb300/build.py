@@ -1,9 +1,11 @@
-"""Build libmoe.so in-tree with nvcc for sm_103a.
+"""Build libmoe.so (and its trace twin libmoe_trace.so) in-tree with nvcc
+for sm_103a.
 
-Each .cu under csrc/ compiles in parallel to an object under _build/, then
-one nvcc link makes combine_moe_plan_gb300/_lib/libmoe.so (CUDA runtime linked
-statically, only the extern "C" API exported).  ptxas register/spill reports
-are kept in _build/ptxas.log.
+Each .cu under csrc/ compiles in parallel to an object under _build/<variant>/,
+then one nvcc link per variant makes combine_moe_plan_gb300/_lib/libmoe.so
+and libmoe_trace.so (the same sources with -DMOE_TRACE: in-kernel stage
+probes).  CUDA runtime linked statically; only the extern "C" API exported.
+ptxas register/spill reports are kept in _build/ptxas.log.
 """
 from __future__ import annotations
 
@@ -21,6 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libmoe.so")
+TRACE_LIB = os.path.join(LIBDIR, "libmoe_trace.so")
+VARIANTS = {"libmoe.so": [], "libmoe_trace.so": ["-DMOE_TRACE"]}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -40,13 +44,14 @@ def _sources():
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        [os.path.join(INCLUDE, "moe.h")]
+        glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    libs = [os.path.join(LIBDIR, v) for v in VARIANTS]
+    if not all(os.path.exists(p) for p in libs):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(p) for p in libs)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
@@ -57,26 +62,33 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *CFLAGS, "-c", src, "-o", obj]
+    def compile_one(job):
+        variant, src = job
+        odir = os.path.join(BUILD, variant.replace(".so", ""))
+        os.makedirs(odir, exist_ok=True)
+        obj = os.path.join(odir, os.path.basename(src) + ".o")
+        cmd = [nvcc, *ARCH, *CFLAGS, *VARIANTS[variant], "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
-        return obj, r.stderr
+        return variant, obj, r.stderr
 
-    srcs = _sources()
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(compile_one, srcs))
+    jobs = [(v, src) for v in VARIANTS for src in _sources()]
+    with cf.ThreadPoolExecutor(max_workers=min(12, len(jobs))) as ex:
+        results = list(ex.map(compile_one, jobs))
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
-        for (obj, log) in results:
-            f.write(f"== {os.path.basename(obj)}\n{log}\n")
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+        for (variant, obj, log) in results:
+            if variant == "libmoe.so":
+                f.write(f"== {os.path.basename(obj)}\n{log}\n")
+    for variant in VARIANTS:
+        out = os.path.join(LIBDIR, variant)
+        tmp = out + f".tmp{os.getpid()}"
+        objs = [o for (v, o, _) in results if v == variant]
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, out)
     if verbose:
         print(open(os.path.join(BUILD, "ptxas.log")).read())
     return LIB

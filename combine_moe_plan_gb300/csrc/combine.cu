@@ -14,6 +14,9 @@
 // loads in flight before it accumulates them in order.
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
+
+MOE_TRACE_BUFFERS(tr_combine)
 
 namespace moe {
 namespace {
@@ -27,8 +30,12 @@ __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ slot,
                const float* __restrict__ gates, int T, int H, int k, uint16_t* __restrict__ y,
                int32_t* __restrict__ err) {
+    // Trace stages (warp 0 of the CTA): 0 start, 1 slots and gates loaded,
+    // 2 accumulation done, 3 output stored.
     grid_dependency_sync();
     allow_dependents();
+    MOE_TRACE_SM(tr_combine);
+    MOE_TRACE_MARK(tr_combine, 0);
     const int lane = threadIdx.x & 31;
     const int segs = (H + kSegElems - 1) / kSegElems;
     const long long item = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
@@ -49,6 +56,7 @@ combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ 
         if (lane == 0) set_error(err, MOE_DEVERR_SLOT);
         return;
     }
+    MOE_TRACE_MARK(tr_combine, 1);
 
     int col[kChunks];
     bool act[kChunks];
@@ -94,6 +102,7 @@ combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ 
         }
     }
 
+    MOE_TRACE_MARK(tr_combine, 2);
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
         if (!act[c]) continue;
@@ -104,9 +113,17 @@ combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ 
         o.w = pack_bf16x2_rn(acc[c][6], acc[c][7]);
         st16(y + (size_t)t * H + col[c], o);
     }
+    MOE_TRACE_MARK(tr_combine, 3);
 }
 
 }  // namespace
+
+#ifdef MOE_TRACE
+int trace_symbols_combine(void** stamps, void** sms) {
+    if (cudaGetSymbolAddress(stamps, tr_combine_t) != cudaSuccess) return -1;
+    return cudaGetSymbolAddress(sms, tr_combine_sm) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 cudaError_t launch_combine(const uint16_t* ex_out, const int32_t* slot, const float* gates, int T, int H, int k,
                            uint16_t* y, int32_t* err, cudaStream_t s, uint64_t* launches) {

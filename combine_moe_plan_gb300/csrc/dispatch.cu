@@ -15,6 +15,9 @@
 // once; every byte of every destination row is written exactly once.
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
+
+MOE_TRACE_BUFFERS(tr_dispatch)
 
 namespace moe {
 namespace {
@@ -36,8 +39,12 @@ __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, f
 __global__ void __launch_bounds__(kDispatchThreads)
 dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ slot,
                 int8_t* __restrict__ codes, float* __restrict__ scales, int Gs, int32_t* __restrict__ err) {
+    // Trace stages (warp 0 of the CTA): 0 start, 1 row and slots loaded,
+    // 2 quantized, 3 stores issued.
     grid_dependency_sync();
     allow_dependents();
+    MOE_TRACE_SM(tr_dispatch);
+    MOE_TRACE_MARK(tr_dispatch, 0);
     const int lane = threadIdx.x & 31;
     const int segs = (H + kSegElems - 1) / kSegElems;
     const long long item = (long long)blockIdx.x * (kDispatchThreads / 32) + (threadIdx.x >> 5);
@@ -70,6 +77,7 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+    MOE_TRACE_MARK(tr_dispatch, 1);
 
     uint4 q;
     q.x = quant4(v[0], v[1], v[2], v[3], amax);
@@ -83,6 +91,7 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32
     sc.y = __shfl_sync(kFull, scale, 8);
     sc.z = __shfl_sync(kFull, scale, 16);
     sc.w = __shfl_sync(kFull, scale, 24);
+    MOE_TRACE_MARK(tr_dispatch, 2);
 
     for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(kFull, my_slot, j);
@@ -95,6 +104,7 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32
     // Scales of this segment's 4 groups: one 16-byte store per destination row.
     if (lane < k && my_slot >= 0 && my_slot < rows && seg * 4 < Gs)
         *reinterpret_cast<float4*>(scales + (size_t)my_slot * Gs + seg * 4) = sc;
+    MOE_TRACE_MARK(tr_dispatch, 3);
 }
 
 constexpr int kExpertThreads = 256;
@@ -131,6 +141,13 @@ identity_experts_kernel(const int8_t* __restrict__ codes, const float* __restric
 }
 
 }  // namespace
+
+#ifdef MOE_TRACE
+int trace_symbols_dispatch(void** stamps, void** sms) {
+    if (cudaGetSymbolAddress(stamps, tr_dispatch_t) != cudaSuccess) return -1;
+    return cudaGetSymbolAddress(sms, tr_dispatch_sm) == cudaSuccess ? 0 : -1;
+}
+#endif
 
 cudaError_t launch_dispatch(const uint16_t* x, int T, int H, int k, const int32_t* slot, int8_t* codes,
                             float* scales, int Gs, int32_t* err, cudaStream_t s, uint64_t* launches) {

@@ -28,6 +28,8 @@ struct Geometry {
     int32_t Gs;          // G rounded up to a multiple of 4 (16-byte scale rows)
     int32_t tiles_max;   // ceil(T_max / kTileTokens)
     size_t error_word;   // offset of the shared device error word
+    size_t ticket;       // offset of n_sets int32 plan tickets (single-launch plan)
+    size_t control_bytes;// error word + tickets, zeroed by moe_pool_clear_error
     SetLayout set[kMaxSets];
     size_t total;
 };
@@ -61,6 +63,7 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k,
                         int32_t* tile_hist, int32_t* local_rank,
                         int32_t* counts, int32_t* offsets, int32_t* slot,
                         int32_t* src_token, int32_t* src_k, int32_t* err,
+                        int32_t* ticket /* zeroed int32, or NULL: always three launches */,
                         cudaStream_t s, uint64_t* launches);
 
 cudaError_t launch_dispatch(const uint16_t* x, int T, int H, int k, const int32_t* slot,

@@ -7,7 +7,7 @@
 // generation and token reordering before dispatch).  StrataCL analysis,
 // section 3.5: token placement -> expert-window aggregation.
 //
-// Three launches:
+// Three launches for large batches (one for small ones, see plan_single_kernel):
 //   route_tile   one CTA of 32 warps per tile of 32 tokens, one warp per
 //                token: k rounds of shuffle arg-max (ties -> lower expert
 //                id).  The CTA then computes the gates in fp64 with one
@@ -28,11 +28,33 @@
 
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
+
+MOE_TRACE_BUFFERS(tr_route)
+MOE_TRACE_BUFFERS(tr_single)
+MOE_TRACE_BUFFERS(tr_scan)
+MOE_TRACE_BUFFERS(tr_assign)
 
 namespace moe {
 namespace {
 
+#ifdef MOE_TRACE
+// Stage stamps of route_tile go to the slice of the kernel that called it.
+template <bool SINGLE>
+__device__ __forceinline__ TraceSlice route_slice() {
+    return SINGLE ? tr_single_t : tr_route_t;
+}
+#define ROUTE_MARK(stage) trace_mark(route_slice<SINGLE>(), (stage))
+#else
+#define ROUTE_MARK(stage) ((void)0)
+#endif
+
 constexpr int kRouteThreads = 32 * kTileTokens;  // one warp per token of the tile
+
+// Batches of at most this many 32-token tiles are planned in one launch.
+#ifndef MOE_PLAN_SINGLE_MAX_TILES
+#define MOE_PLAN_SINGLE_MAX_TILES 32
+#endif
 
 // Monotone map of finite floats onto uint32 (a < b  <=>  key(a) < key(b));
 // -0 is folded onto +0 first, so equal values give equal keys.  Every finite
@@ -43,14 +65,17 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-template <int EPL>  // logits per lane = ceil(E / 32)
-__global__ void __launch_bounds__(kRouteThreads)
-route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
-                  const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
-                  int32_t* __restrict__ topk_e, float* __restrict__ gates,
-                  int32_t* __restrict__ phys, int32_t* __restrict__ tile_hist, int n_tiles,
-                  int32_t* __restrict__ local_rank, int32_t* __restrict__ err) {
-    extern __shared__ __align__(16) unsigned char smem[];
+// Route one 32-token tile (the body shared by both plan variants).
+// Trace stages: 0 start, 1 top-k done, 2 exp done, 3 sums done, 4 gates and
+// masks done, 5 tile counts and ranks written.
+template <int EPL, bool SINGLE>  // logits per lane = ceil(E / 32)
+__device__ __forceinline__ void route_tile(const float* __restrict__ logits, int T, int E, int P, int k,
+                                           const int32_t* __restrict__ rep_off,
+                                           const int32_t* __restrict__ rep_ids, int32_t* __restrict__ topk_e,
+                                           float* __restrict__ gates, int32_t* __restrict__ phys,
+                                           int32_t* __restrict__ tile_hist, int n_tiles,
+                                           int32_t* __restrict__ local_rank, int32_t* __restrict__ err,
+                                           unsigned char* smem, int tile) {
     double* e64 = reinterpret_cast<double*>(smem);                          // [32*k]
     double* rsum = e64 + kTileTokens * k;                                   // [32] 1 / sum per token
     float* sel_v = reinterpret_cast<float*>(rsum + kTileTokens);            // [32*k]
@@ -60,9 +85,7 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     int32_t* s_off = reinterpret_cast<int32_t*>(mask + P);                 // [E+1] replica CSR
     int32_t* s_ids = s_off + (E + 1);                                       // [P]
 
-    grid_dependency_sync();
-    allow_dependents();
-    const int tile = blockIdx.x;
+    ROUTE_MARK(0);
     const int tl = threadIdx.x >> 5;  // this warp's token within the tile
     const int lane = threadIdx.x & 31;
     const int t0 = tile * kTileTokens;
@@ -115,6 +138,7 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
         }
     }
     __syncthreads();
+    ROUTE_MARK(1);
 
     // ---- gates in fp64: e_j = exp(l_j - l_0) (e_0 = 1 exactly), s = sum over
     // j ascending, gate = (float)(e_j / s) computed as e_j * (1 / s) ----
@@ -125,12 +149,14 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     const bool item_ok = it < n_items && t0 + itl < T;
     if (item_ok) e64[it] = (ij == 0) ? 1.0 : exp((double)sel_v[it] - (double)sel_v[itl * k]);
     __syncthreads();
+    ROUTE_MARK(2);
     if (threadIdx.x < kTileTokens && t0 + (int)threadIdx.x < T) {
         double s = 0.0;
         for (int jj = 0; jj < k; ++jj) s += e64[threadIdx.x * k + jj];
         rsum[threadIdx.x] = 1.0 / s;
     }
     __syncthreads();
+    ROUTE_MARK(3);
     if (item_ok) {
         const int tt = t0 + itl;
         const float g = (float)(e64[it] * rsum[itl]);
@@ -159,6 +185,7 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
         }
     }
     __syncthreads();
+    ROUTE_MARK(4);
 
     // ---- tile histogram (expert-major) and in-tile ranks ----
     for (int p = threadIdx.x; p < P; p += kRouteThreads)
@@ -167,20 +194,31 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
         const int p = sel_p[it];
         local_rank[(size_t)(t0 + itl) * k + ij] = (p >= 0) ? __popc(mask[p] & ((1u << itl) - 1u)) : 0;
     }
+    ROUTE_MARK(5);
 }
 
-// One warp per physical expert p: exclusive scan of tile_hist[p, :] in place,
-// counts[p] = column total.
+template <int EPL>
+__global__ void __launch_bounds__(kRouteThreads)
+route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
+                  const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
+                  int32_t* __restrict__ topk_e, float* __restrict__ gates,
+                  int32_t* __restrict__ phys, int32_t* __restrict__ tile_hist, int n_tiles,
+                  int32_t* __restrict__ local_rank, int32_t* __restrict__ err) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    grid_dependency_sync();
+    allow_dependents();
+    MOE_TRACE_SM(tr_route);
+    route_tile<EPL, false>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles,
+                           local_rank, err, smem, blockIdx.x);
+}
+
+// One warp: exclusive scan of tile_hist[p, :] in place, counts[p] = column
+// total.  Loads bypass L1 (the counts may come from other CTAs of the launch).
 constexpr int kScanThreads = 256;
 constexpr int kScanBatch = 8;  // chunks of 32 tiles loaded before scanning
 
-__global__ void __launch_bounds__(kScanThreads)
-column_scan_kernel(int32_t* __restrict__ tile_hist, int n_tiles, int P, int32_t* __restrict__ counts) {
-    grid_dependency_sync();
-    allow_dependents();
-    const int p = blockIdx.x * (kScanThreads / 32) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (p >= P) return;
+__device__ __forceinline__ void scan_column(int32_t* __restrict__ tile_hist, int n_tiles, int p, int lane,
+                                            int32_t* __restrict__ counts) {
     int32_t* col = tile_hist + (size_t)p * n_tiles;
     int carry = 0;
     for (int base = 0; base < n_tiles; base += 32 * kScanBatch) {
@@ -188,7 +226,7 @@ column_scan_kernel(int32_t* __restrict__ tile_hist, int n_tiles, int P, int32_t*
 #pragma unroll
         for (int u = 0; u < kScanBatch; ++u) {
             const int idx = base + u * 32 + lane;
-            v[u] = (idx < n_tiles) ? col[idx] : 0;
+            v[u] = (idx < n_tiles) ? __ldcg(col + idx) : 0;
         }
 #pragma unroll
         for (int u = 0; u < kScanBatch; ++u) {
@@ -206,6 +244,17 @@ column_scan_kernel(int32_t* __restrict__ tile_hist, int n_tiles, int P, int32_t*
     if (lane == 0) counts[p] = carry;
 }
 
+__global__ void __launch_bounds__(kScanThreads)
+column_scan_kernel(int32_t* __restrict__ tile_hist, int n_tiles, int P, int32_t* __restrict__ counts) {
+    grid_dependency_sync();
+    allow_dependents();
+    MOE_TRACE_SM(tr_scan);
+    MOE_TRACE_MARK(tr_scan, 0);
+    const int p = blockIdx.x * (kScanThreads / 32) + (threadIdx.x >> 5);
+    if (p < P) scan_column(tile_hist, n_tiles, p, threadIdx.x & 31, counts);
+    MOE_TRACE_MARK(tr_scan, 1);
+}
+
 // Exclusive scan of counts[0..P) into offs[0..P] in shared memory (whole CTA).
 template <int THREADS>
 __device__ void block_offsets(const int32_t* __restrict__ counts, int P, int32_t* offs) {
@@ -214,7 +263,7 @@ __device__ void block_offsets(const int32_t* __restrict__ counts, int P, int32_t
     const int lo = threadIdx.x * per;
     int local = 0;
     for (int i = 0; i < per; ++i)
-        if (lo + i < P) local += counts[lo + i];
+        if (lo + i < P) local += __ldcg(counts + lo + i);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = local;
 #pragma unroll
@@ -230,7 +279,7 @@ __device__ void block_offsets(const int32_t* __restrict__ counts, int P, int32_t
     for (int i = 0; i < per; ++i) {
         if (lo + i < P) {
             offs[lo + i] = run;
-            run += counts[lo + i];
+            run += __ldcg(counts + lo + i);
         }
     }
     if (threadIdx.x == THREADS - 1) offs[P] = wbase + incl;
@@ -247,6 +296,8 @@ assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile
     extern __shared__ int32_t offs[];  // [P+1]
     grid_dependency_sync();
     allow_dependents();
+    MOE_TRACE_SM(tr_assign);
+    MOE_TRACE_MARK(tr_assign, 0);
     const int n = T * k;
     const int it = blockIdx.x * kAssignThreads + threadIdx.x;
     // Loads that do not depend on the offsets go out before the block scan.
@@ -257,9 +308,13 @@ assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile
         if (p >= 0 && p < P) base = tile_hist[(size_t)p * n_tiles + (it / k) / kTileTokens];
     }
     block_offsets<kAssignThreads>(counts, P, offs);
+    MOE_TRACE_MARK(tr_assign, 1);
     if (blockIdx.x == 0)
         for (int q = threadIdx.x; q <= P; q += kAssignThreads) offsets[q] = offs[q];
-    if (it >= n) return;
+    if (it >= n) {
+        MOE_TRACE_MARK(tr_assign, 2);
+        return;
+    }
     const int t = it / k;
     const int j = it - t * k;
     int r = -1;
@@ -274,45 +329,104 @@ assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile
     src_k[r] = j;
 }
 
+// Single-launch plan for batches of at most MOE_PLAN_SINGLE_MAX_TILES tiles
+// (trace stages 0-5 as route_tile; the last CTA adds 6 scans done, 7 end)
+// (the decode regime): every CTA routes its tile; the CTA that finishes last
+// (atomic ticket, no waiting) then runs the column scans, the offsets and the
+// slot assignment for the whole batch, and resets the ticket for the next
+// call.  Each CTA fences its writes before taking its ticket, and the last
+// one reads the others' results with L1-bypassing loads.
 template <int EPL>
-cudaError_t launch_route(dim3 grid, size_t smem, cudaStream_t s, const float* logits, int T, int E,
-                         int P, int k, const int32_t* rep_off, const int32_t* rep_ids, int32_t* topk_e,
-                         float* gates, int32_t* phys, int32_t* tile_hist, int n_tiles,
-                         int32_t* local_rank, int32_t* err) {
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(route_tile_kernel<EPL>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+__global__ void __launch_bounds__(kRouteThreads)
+plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
+                   const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
+                   int32_t* __restrict__ topk_e, float* __restrict__ gates, int32_t* __restrict__ phys,
+                   int32_t* __restrict__ tile_hist, int n_tiles, int32_t* __restrict__ local_rank,
+                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
+                   int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err,
+                   int32_t* __restrict__ ticket) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int last;
+    grid_dependency_sync();
+    allow_dependents();
+    MOE_TRACE_SM(tr_single);
+    route_tile<EPL, true>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles,
+                          local_rank, err, smem, blockIdx.x);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = (atomicAdd(ticket, 1) == (int)gridDim.x - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+
+    // Column scans, one thread per expert (at most MOE_PLAN_SINGLE_MAX_TILES
+    // entries each): the loads of a column go out together, then a running sum.
+    for (int p = threadIdx.x; p < P; p += kRouteThreads) {
+        int32_t* col = tile_hist + (size_t)p * n_tiles;
+        int carry = 0;
+        for (int base = 0; base < n_tiles; base += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = (base + u < n_tiles) ? __ldcg(col + base + u) : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (base + u < n_tiles) col[base + u] = carry;
+                carry += v[u];
+            }
+        }
+        counts[p] = carry;
     }
-    return launch_pdl(route_tile_kernel<EPL>, grid, dim3(kRouteThreads), smem, s, logits, T, E, P, k, rep_off,
-                      rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, err);
+    __syncthreads();
+    MOE_TRACE_MARK(tr_single, 6);
+    int32_t* offs = reinterpret_cast<int32_t*>(smem);  // [P+1], reuses the route scratch
+    block_offsets<kRouteThreads>(counts, P, offs);
+    for (int q = threadIdx.x; q <= P; q += kRouteThreads) offsets[q] = offs[q];
+    const int n = T * k;
+    for (int it = threadIdx.x; it < n; it += kRouteThreads) {
+        const int t = it / k;
+        const int j = it - t * k;
+        const int p = __ldcg(phys + it);
+        int r = -1;
+        if (p >= 0 && p < P)
+            r = offs[p] + __ldcg(tile_hist + (size_t)p * n_tiles + t / kTileTokens) + __ldcg(local_rank + it);
+        if (r < 0 || r >= n) {
+            set_error(err, MOE_DEVERR_SLOT);
+            slot[it] = -1;
+            continue;
+        }
+        slot[it] = r;
+        src_token[r] = t;
+        src_k[r] = j;
+    }
+    if (threadIdx.x == 0) *ticket = 0;
+    MOE_TRACE_MARK(tr_single, 7);
 }
 
-}  // namespace
+template <typename K>
+cudaError_t smem_attr(K kernel, size_t smem) {
+    if (smem <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
 
-cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
-                        const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys,
-                        int32_t* tile_hist, int32_t* local_rank, int32_t* counts, int32_t* offsets,
-                        int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err,
-                        cudaStream_t s, uint64_t* launches) {
+template <int EPL>
+cudaError_t launch_plan_epl(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
+                            const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys,
+                            int32_t* tile_hist, int32_t* local_rank, int32_t* counts, int32_t* offsets,
+                            int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err, int32_t* ticket,
+                            size_t smem, cudaStream_t s, uint64_t* launches) {
     const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
-    const size_t items = (size_t)kTileTokens * k;
-    const size_t smem = items * (sizeof(double) + sizeof(float) + 2 * sizeof(int32_t)) +
-                        kTileTokens * sizeof(double) + (size_t)P * sizeof(uint32_t) +
-                        (size_t)(E + 1 + P) * sizeof(int32_t);
-    const int epl = (E + 31) / 32;
     cudaError_t e;
-    const dim3 grid(n_tiles);
-#define MOE_ROUTE_CASE(N)                                                                          \
-    e = launch_route<N>(grid, smem, s, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, \
-                        tile_hist, n_tiles, local_rank, err)
-    if (epl <= 1) MOE_ROUTE_CASE(1);
-    else if (epl <= 2) MOE_ROUTE_CASE(2);
-    else if (epl <= 4) MOE_ROUTE_CASE(4);
-    else if (epl <= 8) MOE_ROUTE_CASE(8);
-    else if (epl <= 16) MOE_ROUTE_CASE(16);
-    else MOE_ROUTE_CASE(32);
-#undef MOE_ROUTE_CASE
+    if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
+        if ((e = smem_attr(plan_single_kernel<EPL>, smem)) != cudaSuccess) return e;
+        e = launch_pdl(plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem, s, logits, T, E, P, k,
+                       rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, counts, offsets,
+                       slot, src_token, src_k, err, ticket);
+        if (e == cudaSuccess) *launches += 1;
+        return e;
+    }
+    if ((e = smem_attr(route_tile_kernel<EPL>, smem)) != cudaSuccess) return e;
+    e = launch_pdl(route_tile_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem, s, logits, T, E, P, k,
+                   rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, err);
     if (e != cudaSuccess) return e;
     *launches += 1;
 
@@ -328,6 +442,57 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
     if (e != cudaSuccess) return e;
     *launches += 1;
     return cudaSuccess;
+}
+
+}  // namespace
+
+#ifdef MOE_TRACE
+int trace_symbols_plan(int kind, void** stamps, void** sms) {
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (kind) {
+        case kTraceRoute:
+            e = cudaGetSymbolAddress(stamps, tr_route_t);
+            if (e == cudaSuccess) e = cudaGetSymbolAddress(sms, tr_route_sm);
+            break;
+        case kTraceColumnScan:
+            e = cudaGetSymbolAddress(stamps, tr_scan_t);
+            if (e == cudaSuccess) e = cudaGetSymbolAddress(sms, tr_scan_sm);
+            break;
+        case kTraceAssign:
+            e = cudaGetSymbolAddress(stamps, tr_assign_t);
+            if (e == cudaSuccess) e = cudaGetSymbolAddress(sms, tr_assign_sm);
+            break;
+        case kTracePlanSingle:
+            e = cudaGetSymbolAddress(stamps, tr_single_t);
+            if (e == cudaSuccess) e = cudaGetSymbolAddress(sms, tr_single_sm);
+            break;
+        default:
+            break;
+    }
+    return e == cudaSuccess ? 0 : -1;
+}
+#endif
+
+cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
+                        const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys,
+                        int32_t* tile_hist, int32_t* local_rank, int32_t* counts, int32_t* offsets,
+                        int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err, int32_t* ticket,
+                        cudaStream_t s, uint64_t* launches) {
+    const size_t items = (size_t)kTileTokens * k;
+    size_t smem = items * (sizeof(double) + sizeof(float) + 2 * sizeof(int32_t)) + kTileTokens * sizeof(double) +
+                  (size_t)P * sizeof(uint32_t) + (size_t)(E + 1 + P) * sizeof(int32_t);
+    const int epl = (E + 31) / 32;
+#define MOE_PLAN_CASE(N)                                                                                  \
+    return launch_plan_epl<N>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,      \
+                              local_rank, counts, offsets, slot, src_token, src_k, err, ticket, smem, s, \
+                              launches)
+    if (epl <= 1) MOE_PLAN_CASE(1);
+    if (epl <= 2) MOE_PLAN_CASE(2);
+    if (epl <= 4) MOE_PLAN_CASE(4);
+    if (epl <= 8) MOE_PLAN_CASE(8);
+    if (epl <= 16) MOE_PLAN_CASE(16);
+    MOE_PLAN_CASE(32);
+#undef MOE_PLAN_CASE
 }
 
 }  // namespace moe

@@ -88,7 +88,7 @@ extern "C" MOE_API int moe_plan_static(const float* logits, int32_t T, int32_t E
     int32_t* local_rank = reinterpret_cast<int32_t*>(static_cast<char*>(base) + hist_bytes);
     uint64_t launches = 0;
     cudaError_t e = moe::launch_plan(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
-                                     local_rank, counts, offsets, slot, src_token, src_k, error_word,
+                                     local_rank, counts, offsets, slot, src_token, src_k, error_word, nullptr,
                                      static_cast<cudaStream_t>(stream), &launches);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -52,7 +52,11 @@ int make_geometry(const moe_desc* d, Geometry* g) {
         off = align_up(off + bytes, kAlign);
         return o;
     };
-    g->error_word = take(sizeof(int32_t));
+    // Control block: error word, then one plan ticket per set.
+    g->error_word = 0;
+    g->ticket = 16;
+    g->control_bytes = g->ticket + (size_t)d->n_sets * sizeof(int32_t);
+    take(g->control_bytes);
     const size_t R = (size_t)g->rows, H = (size_t)d->H, T = (size_t)d->T_max, k = (size_t)d->k;
     for (int s = 0; s < d->n_sets; ++s) {
         SetLayout& L = g->set[s];
@@ -155,8 +159,7 @@ MOE_API int moe_pool_view(const moe_pool* pool, int buf, moe_view* v) {
 
 MOE_API int moe_pool_clear_error(moe_pool* pool, void* stream) {
     if (pool == nullptr) return MOE_ERR_NULL;
-    return cuda_rc(cudaMemsetAsync(at<int32_t>(pool, pool->geo.error_word), 0, sizeof(int32_t),
-                                   static_cast<cudaStream_t>(stream)));
+    return cuda_rc(cudaMemsetAsync(pool->base, 0, pool->geo.control_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 MOE_API int moe_pool_check(moe_pool* pool, void* stream, int32_t* error_word) {
@@ -210,7 +213,8 @@ MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T, const int32
                                 at<int32_t>(pool, L.counts), at<int32_t>(pool, L.offsets),
                                 at<int32_t>(pool, L.slot), at<int32_t>(pool, L.src_token),
                                 at<int32_t>(pool, L.src_k), at<int32_t>(pool, pool->geo.error_word),
-                                static_cast<cudaStream_t>(stream), &pool->launches);
+                                at<int32_t>(pool, pool->geo.ticket) + buf, static_cast<cudaStream_t>(stream),
+                                &pool->launches);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     pool->planned_T[buf] = T;
     return MOE_OK;

@@ -46,15 +46,25 @@ class View(ctypes.Structure):
 
 
 _lib = None
+_lib_path = LIB_PATH
+
+
+def use_library(path: str) -> None:
+    """Choose which build of the library this process loads (e.g. the trace
+    build, libmoe_trace.so).  Must be called before the first call into it."""
+    global _lib_path
+    if _lib is not None and path != _lib_path:
+        raise RuntimeError(f"{_lib_path} is already loaded in this process")
+    _lib_path = path
 
 
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise LibraryMissing(f"{LIB_PATH} is not built; run combine_moe_plan_gb300.build.build()")
-    L = ctypes.CDLL(LIB_PATH)
+    if not os.path.exists(_lib_path):
+        raise LibraryMissing(f"{_lib_path} is not built; run combine_moe_plan_gb300.build.build()")
+    L = ctypes.CDLL(_lib_path)
     vp, i32, pp = ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER
     sig = {
         "moe_pool_bytes": [pp(Desc), pp(ctypes.c_size_t)],
@@ -83,7 +93,7 @@ def lib() -> ctypes.CDLL:
 
 
 def header_functions(path: str = HEADER) -> list[str]:
-    """Names of every function include/moe.h declares."""
+    """Names of every function a header (default include/moe.h) declares."""
     src = open(path).read()
     return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)
 

@@ -1,0 +1,132 @@
+"""Stage timelines from the in-kernel probes of libmoe_trace.so.
+
+The trace build stamps, for thread 0 of every CTA, %globaltimer and clock64
+at each stage boundary of each kernel (include/moe_trace.h lists the stages).
+This module loads that build, runs one pass of the path on the GPU, and turns
+the stamps into per-stage durations across CTAs and the span of each launch
+(first CTA start to last CTA end).
+
+    python -m combine_moe_plan_gb300.trace --workload t96_h7168_e256_k8
+
+The probes themselves live in the kernels; nothing here computes any part of
+the method.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import sys
+
+import numpy as np
+
+from combine_moe_plan_gb300 import build as moe_build
+from combine_moe_plan_gb300 import moe
+
+TRACE_CTAS, TRACE_STAGES = 8192, 8
+KINDS = {
+    0: ("route_tile", ["start", "top-k", "exp", "sums", "gates+masks", "counts+ranks"]),
+    1: ("column_scan", ["start", "end"]),
+    2: ("assign", ["start", "offsets", "end"]),
+    3: ("plan_single", ["start", "top-k", "exp", "sums", "gates+masks", "counts+ranks", "scans(last)",
+                        "end(last)"]),
+    4: ("dispatch", ["start", "loaded", "quantized", "stored"]),
+    5: ("combine", ["start", "slots", "accumulated", "stored"]),
+}
+
+
+def load() -> ctypes.CDLL:
+    moe_build.build()
+    moe.use_library(moe_build.TRACE_LIB)
+    L = moe.lib()
+    L.moe_trace_reset.argtypes = [ctypes.c_void_p]
+    L.moe_trace_reset.restype = ctypes.c_int
+    L.moe_trace_read.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    L.moe_trace_read.restype = ctypes.c_int
+    return L
+
+
+def reset(stream=None) -> None:
+    rc = moe.lib().moe_trace_reset(moe._stream(stream))
+    if rc != 0:
+        raise moe.MoeError("moe_trace_reset", rc, "")
+
+
+def read(kind: int):
+    """(stamps uint64 [CTAs, stages, 2] as (ns, cycles), sm uint32 [CTAs])."""
+    stamps = np.zeros((TRACE_CTAS, TRACE_STAGES, 2), np.uint64)
+    sm = np.zeros(TRACE_CTAS, np.uint32)
+    rc = moe.lib().moe_trace_read(kind, stamps.ctypes.data_as(ctypes.c_void_p), sm.ctypes.data_as(ctypes.c_void_p))
+    if rc != 0:
+        raise moe.MoeError("moe_trace_read", rc, "")
+    return stamps, sm
+
+
+def summarize(kind: int, n_ctas: int) -> dict:
+    """Per-stage durations (ns) across the first n_ctas CTAs of the last launch
+    of `kind`: median and 90th percentile of (stamp[s] - stamp[s-1]) over CTAs
+    that reached stage s, plus the launch span and the SMs used."""
+    name, stages = KINDS[kind]
+    st, sm = read(kind)
+    ns = st[:n_ctas, :, 0].astype(np.int64)
+    out = {"kernel": name, "ctas": int(n_ctas), "sms": int(len(np.unique(sm[:n_ctas]))), "stages": {}}
+    for s in range(1, len(stages)):
+        ok = (ns[:, s] > 0) & (ns[:, s - 1] > 0)
+        if ok.any():
+            d = ns[ok, s] - ns[ok, s - 1]
+            out["stages"][f"{stages[s - 1]}->{stages[s]}"] = {
+                "median_ns": float(np.median(d)), "p90_ns": float(np.percentile(d, 90)), "ctas": int(ok.sum())}
+    started = ns[:, 0][ns[:, 0] > 0]
+    last = ns.max(axis=1)
+    if started.size:
+        out["span_ns"] = float(last.max() - started.min())
+        out["cta_ns_median"] = float(np.median(last[ns[:, 0] > 0] - started))
+    return out
+
+
+def run(workload: str, seed: int = 0) -> list:
+    """One plan + dispatch + combine of `workload` under the trace build."""
+    import torch
+    from combine_moe_plan_gb300 import workloads as wl
+    load()
+    w = wl.WORKLOADS[workload]
+    inp = wl.make_inputs(w, seed=seed)
+    dev = torch.device("cuda", 0)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    ro = None if inp["rep_off"] is None else torch.from_numpy(inp["rep_off"]).to(dev)
+    ri = None if inp["rep_ids"] is None else torch.from_numpy(inp["rep_ids"]).to(dev)
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=1, device=dev)
+    if "ex_out" in inp:
+        pool.view(0)["ex_out"][: w.rows].copy_(torch.from_numpy(inp["ex_out"].view(np.int16)).view(torch.bfloat16))
+    y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):  # warm: the last pass is the one read back
+        reset()
+        pool.plan(logits, ro, ri)
+        pool.dispatch(x)
+        pool.combine(w.T, y=y)
+    torch.cuda.synchronize()
+    if pool.check() != 0:
+        raise RuntimeError("device error word set")
+    n_tiles = (w.T + 31) // 32
+    rows = []
+    if n_tiles <= 32:
+        rows.append(summarize(3, n_tiles))
+    else:
+        rows += [summarize(0, n_tiles), summarize(1, (w.P + 7) // 8), summarize(2, (w.rows + 255) // 256)]
+    rows.append(summarize(4, min(TRACE_CTAS, (w.T * ((w.H + 511) // 512) + 7) // 8)))
+    rows.append(summarize(5, min(TRACE_CTAS, (w.T * ((w.H + 255) // 256) + 7) // 8)))
+    return rows
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="t96_h7168_e256_k8")
+    a = ap.parse_args(argv)
+    for r in run(a.workload):
+        print(json.dumps(r))
+
+
+if __name__ == "__main__":
+    main()

@@ -133,7 +133,11 @@ MOE_API int moe_pool_destroy(moe_pool* pool);
 /* Device addresses of buffer set `buf`. */
 MOE_API int moe_pool_view(const moe_pool* pool, int buf, moe_view* view);
 
-/* Zero the device error word (asynchronous on `stream`). */
+/*
+ * Zero the device error word and the pool's plan tickets (asynchronous on
+ * `stream`).  Call once before the pool's first use, and never while the
+ * pool's kernels run on another stream.
+ */
 MOE_API int moe_pool_clear_error(moe_pool* pool, void* stream);
 
 /*

@@ -32,6 +32,19 @@ def test_exports_every_header_symbol(L):
     assert exported == set(names)
 
 
+def test_trace_build_exports_probe_api(L):
+    """libmoe_trace.so exports moe.h plus moe_trace.h; libmoe.so exports no
+    probe entry point."""
+    import os
+    import subprocess
+    from combine_moe_plan_gb300 import build as b
+    trace_names = moe.header_functions(os.path.join(os.path.dirname(moe.HEADER), "moe_trace.h"))
+    assert trace_names == ["moe_trace_reset", "moe_trace_read"]
+    out = subprocess.run(["nm", "-D", "--defined-only", b.TRACE_LIB], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T moe_" in ln}
+    assert exported == set(moe.header_functions()) | set(trace_names)
+
+
 def test_status_strings(L):
     for rc in moe.STATUS:
         assert L.moe_status_str(rc)

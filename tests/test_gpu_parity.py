@@ -251,5 +251,13 @@ def test_launch_count():
     pool = moe.Pool(64, w.H, w.E, w.P, w.k)
     n0 = pool.launches()
     Run(w, inp, pool=pool)
-    # plan = route + column scan + assign; then dispatch, identity experts, combine
+    # a 64-token plan is one launch (two tiles); then dispatch, identity experts, combine
+    assert pool.launches() - n0 == 4
+    # a 1056-token plan (33 tiles) takes the three-launch path
+    big = wl.small_variant(wl.WORKLOADS["t64_h256_e8_k2"], 1056)
+    inp = wl.make_inputs(big, with_expert_out=False)
+    pool = moe.Pool(big.T, big.H, big.E, big.P, big.k)
+    n0 = pool.launches()
+    Run(big, inp, pool=pool)
     assert pool.launches() - n0 == 6
+    _check_all(big, inp, Run(big, inp, pool=pool))
