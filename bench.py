@@ -15,6 +15,9 @@ Phases:
   C  e2e: moe_step_host from pinned host buffers -- logits and x copied in,
      plan, dispatch, identity experts (the device stand-in for the expert
      FFNs), combine, y copied out -- also on the two sets/streams.
+  D  decode latency: the 96-token decode batch (hidden 7168, 256 experts,
+     top-8): plan+dispatch, combine, and the whole layer each captured in a
+     CUDA graph and replayed from an idle GPU; median of the replays.
 
 Prints ONE JSON line (rank 0).
 
@@ -222,6 +225,59 @@ class _Streams:
             self.main.wait_event(e)
 
 
+def decode_latency(dev, reps=200):
+    """Median GPU time of plan+dispatch (the routing metadata is part of the
+    fused dispatch) and of combine, each replayed as a CUDA graph, for the
+    96-token decode batch."""
+    import torch
+    from combine_moe_plan_gb300 import moe
+    w = wl.WORKLOADS["t96_h7168_e256_k8"]
+    inp = wl.make_inputs(w)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=1, device=dev)
+    pool.view(0)["ex_out"][: w.rows].copy_(torch.from_numpy(inp["ex_out"].view(np.int16)).view(torch.bfloat16))
+    y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            pool.plan(logits, stream=s)
+            pool.dispatch(x, stream=s)
+            pool.combine(w.T, y=y, stream=s)
+    torch.cuda.synchronize()
+    g_disp, g_comb, g_layer = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_disp, stream=s):
+        pool.plan(logits, stream=s)
+        pool.dispatch(x, stream=s)
+    with torch.cuda.graph(g_comb, stream=s):
+        pool.combine(w.T, y=y, stream=s)
+    with torch.cuda.graph(g_layer, stream=s):
+        pool.plan(logits, stream=s)
+        pool.dispatch(x, stream=s)
+        pool.combine(w.T, y=y, stream=s)
+    torch.cuda.synchronize()
+
+    def med(fn):
+        ts = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    out = {"workload": w.name, "dispatch_us": med(g_disp.replay), "combine_us": med(g_comb.replay),
+           "layer_us": med(g_layer.replay),
+           "note": "CUDA-graph replays from an idle GPU; dispatch = plan + dispatch (the fused "
+                   "dispatch carries the routing metadata); each graph launch adds its own overhead"}
+    if pool.check() != 0:
+        raise RuntimeError("device error word set in the decode-latency pass")
+    return out
+
+
 def run_ours(a, w: wl.Workload):
     import torch
     import torch.distributed as dist
@@ -318,6 +374,9 @@ def run_ours(a, w: wl.Workload):
     if not a.no_e2e:
         e2e_ms = _e2e(a, w, inp, pool, rep_off, rep_ids, st, ws)
 
+    # ---- phase D: decode-batch latency (CUDA graphs) ----
+    decode = None if a.no_e2e else decode_latency(dev)
+
     # ---- max over ranks ----
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev)
     if rank == 0:
@@ -356,6 +415,7 @@ def run_ours(a, w: wl.Workload):
                         "stand-in for the expert FFNs), combine, y device->host; two sets on two streams"},
             "gpu_launches": int(launches),
             "clocks": clocks,
+            "decode_latency": decode,
         }
         if not a.no_cpu_baseline and ws == 1:
             out["cpu_baseline"] = cpu_baseline(w, inp)

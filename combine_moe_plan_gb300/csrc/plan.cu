@@ -38,6 +38,52 @@ MOE_TRACE_BUFFERS(tr_assign)
 namespace moe {
 namespace {
 
+// Largest key of a lane and its slot r (the lowest r among equal keys): a
+// tree over adjacent pairs, so the left (lower-r) side wins ties.
+template <int N>
+__device__ __forceinline__ void lane_max(const uint32_t (&key)[N], uint32_t& m, int& r) {
+    uint32_t v[N];
+    int id[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        v[i] = key[i];
+        id[i] = i;
+    }
+#pragma unroll
+    for (int w = N / 2; w >= 1; w /= 2) {
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const bool take = v[2 * i + 1] > v[2 * i];
+            v[i] = take ? v[2 * i + 1] : v[2 * i];
+            id[i] = take ? id[2 * i + 1] : id[2 * i];
+        }
+    }
+    m = v[0];
+    r = id[0];
+}
+
+// The two largest keys of a lane and their slots (lower slot first among
+// equal keys); k2 = 0 if the lane has fewer than two keys above 0.
+template <int N>
+__device__ __forceinline__ void lane_top2(const uint32_t (&key)[N], uint32_t& k1, int& r1, uint32_t& k2, int& r2) {
+    k1 = 0u;
+    r1 = 0;
+    k2 = 0u;
+    r2 = 0;
+#pragma unroll
+    for (int r = 0; r < N; ++r) {
+        if (key[r] > k1) {
+            k2 = k1;
+            r2 = r1;
+            k1 = key[r];
+            r1 = r;
+        } else if (key[r] > k2) {
+            k2 = key[r];
+            r2 = r;
+        }
+    }
+}
+
 #ifdef MOE_TRACE
 // Stage stamps of route_tile go to the slice of the kernel that called it.
 template <bool SINGLE>
@@ -91,18 +137,30 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     const int t0 = tile * kTileTokens;
     const int t = t0 + tl;
 
-    for (int p = threadIdx.x; p < P; p += kRouteThreads) mask[p] = 0u;
-    if (rep_off != nullptr) {
-        for (int i = threadIdx.x; i <= E; i += kRouteThreads) s_off[i] = rep_off[i];
-        for (int i = threadIdx.x; i < P; i += kRouteThreads) s_ids[i] = rep_ids[i];
-    }
 
     // ---- top-k of token t: k rounds of warp arg-max, ties -> lower id ----
     // Logits become order-preserving unsigned keys (-0 folded onto +0 so that
-    // equal floats give equal keys); a round is a per-lane max, one warp
-    // max-reduction of the key and one min-reduction of the expert id among
-    // the lanes holding that key.  Key 0 sits below every finite logit and
-    // marks padding and experts already taken.
+    // equal floats give equal keys).  Each lane caches its two largest keys;
+    // a round is one warp max-reduction of the lanes' first keys and one
+    // min-reduction of the expert id among the lanes holding the maximum,
+    // after which the winning lane promotes its second key (and rescans only
+    // when it has none left).  Key 0 sits below every finite logit and marks
+    // padding and experts already taken.  The replica map is fetched into
+    // registers before the logits, so both loads are in flight together.
+    int32_t rm_off[2] = {0, 0};        // E + 1 <= 1025 entries
+    int32_t rm_ids[4] = {0, 0, 0, 0};  // P <= 4096 = 4 x kRouteThreads
+    if (rep_off != nullptr) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = q * kRouteThreads + threadIdx.x;
+            if (i <= E) rm_off[q] = __ldg(rep_off + i);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = q * kRouteThreads + threadIdx.x;
+            if (i < P) rm_ids[q] = __ldg(rep_ids + i);
+        }
+    }
     if (t < T) {
         const float* row = logits + (size_t)t * E;
         uint32_t key[EPL];
@@ -111,30 +169,44 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
             const int e = r * 32 + lane;
             key[r] = (e < E) ? order_key(__ldg(row + e)) : 0u;
         }
+        uint32_t k1, k2;
+        int r1, r2;
+        lane_top2(key, k1, r1, k2, r2);
         int my_e = 0;
         for (int j = 0; j < k; ++j) {
-            uint32_t lm = 0u;
-            int li = INT_MAX;
-#pragma unroll
-            for (int r = 0; r < EPL; ++r) {
-                if (key[r] > lm) {  // strict: the lowest r (lowest id) wins a tie
-                    lm = key[r];
-                    li = r * 32 + lane;
-                }
-            }
-            const uint32_t m = __reduce_max_sync(kFull, lm);
-            int win = (int)__reduce_min_sync(kFull, (lm == m) ? (uint32_t)li : (uint32_t)INT_MAX);
+            const uint32_t m = __reduce_max_sync(kFull, k1);
+            int win = (int)__reduce_min_sync(kFull, (k1 == m) ? (uint32_t)(r1 * 32 + lane) : (uint32_t)INT_MAX);
             if (win >= E) win = 0;  // only reachable with NaN logits (outside the domain)
             if (lane == (win & 31)) {
 #pragma unroll
                 for (int r = 0; r < EPL; ++r)
-                    if (r == (win >> 5)) key[r] = 0u;
+                    if (r == r1) key[r] = 0u;
+                if (k2 != 0u) {
+                    k1 = k2;
+                    r1 = r2;
+                    k2 = 0u;
+                } else {
+                    lane_top2(key, k1, r1, k2, r2);
+                }
             }
             if (lane == j) my_e = win;
         }
         if (lane < k) {
             sel_v[tl * k + lane] = __ldg(row + my_e);
             sel_e[tl * k + lane] = my_e;
+        }
+    }
+    for (int p = threadIdx.x; p < P; p += kRouteThreads) mask[p] = 0u;
+    if (rep_off != nullptr) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int i = q * kRouteThreads + threadIdx.x;
+            if (i <= E) s_off[i] = rm_off[q];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = q * kRouteThreads + threadIdx.x;
+            if (i < P) s_ids[i] = rm_ids[q];
         }
     }
     __syncthreads();
@@ -286,6 +358,39 @@ __device__ void block_offsets(const int32_t* __restrict__ counts, int P, int32_t
     __syncthreads();
 }
 
+// In-place exclusive scan of a[0..n) in shared memory by the whole CTA;
+// a[n] receives the total.
+template <int THREADS>
+__device__ void block_scan_in_place(int32_t* a, int n) {
+    __shared__ int32_t warp_tot[THREADS / 32];
+    const int per = (n + THREADS - 1) / THREADS;
+    const int lo = threadIdx.x * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i)
+        if (lo + i < n) local += a[lo + i];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+    int run = wbase + incl - local;
+    for (int i = 0; i < per; ++i) {
+        if (lo + i < n) {
+            const int v = a[lo + i];
+            a[lo + i] = run;
+            run += v;
+        }
+    }
+    if (threadIdx.x == THREADS - 1) a[n] = wbase + incl;
+    __syncthreads();
+}
+
 constexpr int kAssignThreads = 256;
 
 __global__ void __launch_bounds__(kAssignThreads)
@@ -344,7 +449,7 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
                    int32_t* __restrict__ tile_hist, int n_tiles, int32_t* __restrict__ local_rank,
                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
                    int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err,
-                   int32_t* __restrict__ ticket) {
+                   int32_t* __restrict__ ticket, int col_smem) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int last;
     grid_dependency_sync();
@@ -360,9 +465,14 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     __threadfence();
 
     // Column scans, one thread per expert (at most MOE_PLAN_SINGLE_MAX_TILES
-    // entries each): the loads of a column go out together, then a running sum.
+    // entries each): the loads of a column go out together, then a running
+    // sum.  Counts land in shared memory (scanned in place into offsets) and,
+    // when they fit (col_smem), so do the tile bases.
+    int32_t* offs = reinterpret_cast<int32_t*>(smem);  // [P+1], reuses the route scratch
+    int32_t* colpre = offs + (P + 1);                   // [P, n_tiles] when col_smem
     for (int p = threadIdx.x; p < P; p += kRouteThreads) {
         int32_t* col = tile_hist + (size_t)p * n_tiles;
+        int32_t* dst = col_smem ? colpre + (size_t)p * n_tiles : col;
         int carry = 0;
         for (int base = 0; base < n_tiles; base += 8) {
             int v[8];
@@ -370,25 +480,28 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
             for (int u = 0; u < 8; ++u) v[u] = (base + u < n_tiles) ? __ldcg(col + base + u) : 0;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                if (base + u < n_tiles) col[base + u] = carry;
+                if (base + u < n_tiles) dst[base + u] = carry;
                 carry += v[u];
             }
         }
         counts[p] = carry;
+        offs[p] = carry;
     }
     __syncthreads();
     MOE_TRACE_MARK(tr_single, 6);
-    int32_t* offs = reinterpret_cast<int32_t*>(smem);  // [P+1], reuses the route scratch
-    block_offsets<kRouteThreads>(counts, P, offs);
+    block_scan_in_place<kRouteThreads>(offs, P);
     for (int q = threadIdx.x; q <= P; q += kRouteThreads) offsets[q] = offs[q];
     const int n = T * k;
     for (int it = threadIdx.x; it < n; it += kRouteThreads) {
         const int t = it / k;
         const int j = it - t * k;
         const int p = __ldcg(phys + it);
+        const int rank = __ldcg(local_rank + it);
         int r = -1;
-        if (p >= 0 && p < P)
-            r = offs[p] + __ldcg(tile_hist + (size_t)p * n_tiles + t / kTileTokens) + __ldcg(local_rank + it);
+        if (p >= 0 && p < P) {
+            const size_t c = (size_t)p * n_tiles + t / kTileTokens;
+            r = offs[p] + (col_smem ? colpre[c] : __ldcg(tile_hist + c)) + rank;
+        }
         if (r < 0 || r >= n) {
             set_error(err, MOE_DEVERR_SLOT);
             slot[it] = -1;
@@ -401,6 +514,8 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     if (threadIdx.x == 0) *ticket = 0;
     MOE_TRACE_MARK(tr_single, 7);
 }
+
+constexpr size_t kTailSmemMax = 96 * 1024;
 
 template <typename K>
 cudaError_t smem_attr(K kernel, size_t smem) {
@@ -417,10 +532,16 @@ cudaError_t launch_plan_epl(const float* logits, int T, int E, int P, int k, con
     const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
     cudaError_t e;
     if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
-        if ((e = smem_attr(plan_single_kernel<EPL>, smem)) != cudaSuccess) return e;
-        e = launch_pdl(plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem, s, logits, T, E, P, k,
+        // The tail keeps offsets (P+1) and, when they fit, the tile bases
+        // (P x n_tiles) in shared memory.
+        const size_t tail = (size_t)(P + 1 + (size_t)P * n_tiles) * sizeof(int32_t);
+        const int col_smem = tail <= kTailSmemMax ? 1 : 0;
+        size_t need = col_smem ? tail : (size_t)(P + 1) * sizeof(int32_t);
+        const size_t smem1 = smem > need ? smem : need;
+        if ((e = smem_attr(plan_single_kernel<EPL>, smem1)) != cudaSuccess) return e;
+        e = launch_pdl(plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem1, s, logits, T, E, P, k,
                        rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, counts, offsets,
-                       slot, src_token, src_k, err, ticket);
+                       slot, src_token, src_k, err, ticket, col_smem);
         if (e == cudaSuccess) *launches += 1;
         return e;
     }

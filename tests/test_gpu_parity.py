@@ -179,6 +179,27 @@ def test_max_experts_and_max_k():
     _custom(65, 128, 1024, 1024, 32, rng.standard_normal((65, 1024)))
 
 
+def test_max_experts_with_replica_map():
+    """E = 1024 logical experts (1025 CSR offsets) with 76 replicas, P = 1100."""
+    E, P, k, T = 1024, 1100, 8, 70
+    rng = np.random.default_rng(9)
+    hot = rng.choice(E, size=P - E, replace=False)
+    off = np.zeros(E + 1, np.int32)
+    ids = []
+    extra = E
+    for e in range(E):
+        mine = [e]
+        if e in set(hot.tolist()):
+            mine.append(extra)
+            extra += 1
+        ids += mine
+        off[e + 1] = off[e] + len(mine)
+    ids = np.array(ids, np.int32)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[:, hot] += 2.0
+    _custom(T, 128, E, P, k, lg, rep_off=off, rep_ids=ids)
+
+
 def test_three_replicas_and_zero_groups():
     """Expert 0 has three physical replicas; some activation groups are all zero."""
     E, P = 6, 9
