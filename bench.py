@@ -14,7 +14,8 @@ Phases:
      so step i+1's plan overlaps step i's bandwidth-bound kernels.
   C  e2e: moe_step_host from pinned host buffers -- logits and x copied in,
      plan, dispatch, identity experts (the device stand-in for the expert
-     FFNs), combine, y copied out -- also on the two sets/streams.
+     FFNs), combine, y copied out -- on a pool of three sets and three
+     streams (copies in, kernels and copy out of different steps overlap).
   D  decode latency: the 96-token decode batch (hidden 7168, 256 experts,
      top-8): plan+dispatch, combine, and the whole layer each captured in a
      CUDA graph and replayed from an idle GPU; median of the replays.
@@ -201,15 +202,15 @@ def run_reference(a, w: wl.Workload):
 
 
 class _Streams:
-    """Two streams, one per buffer set: step i runs on stream i & 1, so the
+    """One stream per buffer set: step i runs on stream i mod n, so the
     latency-bound plan of step i+1 overlaps the bandwidth-bound kernels of
     step i (the micro-batch overlap the double-buffered pool exists for).
     Each stream only ever touches its own set, so stream order alone keeps
     every set's plan -> dispatch -> combine -> next plan sequence intact."""
 
-    def __init__(self, torch, dev):
+    def __init__(self, torch, dev, n=2):
         self.torch = torch
-        self.s = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+        self.s = [torch.cuda.Stream(device=dev) for _ in range(n)]
         self.main = torch.cuda.current_stream()
 
     def fork(self):
@@ -372,7 +373,9 @@ def run_ours(a, w: wl.Workload):
     # ---- phase C: e2e through moe_step_host from pinned host buffers ----
     e2e_ms = float("nan")
     if not a.no_e2e:
-        e2e_ms = _e2e(a, w, inp, pool, rep_off, rep_ids, st, ws)
+        del pool, ys
+        torch.cuda.empty_cache()
+        e2e_ms = _e2e(a, w, inp, rep_off, rep_ids, dev, ws)
 
     # ---- phase D: decode-batch latency (CUDA graphs) ----
     decode = None if a.no_e2e else decode_latency(dev)
@@ -412,7 +415,7 @@ def run_ours(a, w: wl.Workload):
                 "h2d_bytes_per_step": int(inp["logits"].nbytes + inp["x"].nbytes),
                 "d2h_bytes_per_step": int(w.T * w.H * 2), "ms_per_step": e2e_ms,
                 "path": "moe_step_host: logits+x host->device, plan, dispatch, identity experts (device "
-                        "stand-in for the expert FFNs), combine, y device->host; two sets on two streams"},
+                        "stand-in for the expert FFNs), combine, y device->host; three sets on three streams"},
             "gpu_launches": int(launches),
             "clocks": clocks,
             "decode_latency": decode,
@@ -425,21 +428,30 @@ def run_ours(a, w: wl.Workload):
         dist.destroy_process_group()
 
 
-def _e2e(a, w, inp, pool, rep_off, rep_ids, st, ws):
-    """ms per step of moe_step_host from pinned host buffers (copies inside)."""
+E2E_SETS = 3
+
+
+def _e2e(a, w, inp, rep_off, rep_ids, dev, ws):
+    """ms per step of moe_step_host from pinned host buffers (copies inside).
+    A pool of three buffer sets on three streams: one set's host copies,
+    another's kernels and a third's copy back proceed together."""
     import torch
     import torch.distributed as dist
+    from combine_moe_plan_gb300 import moe
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=E2E_SETS, device=dev)
+    st = _Streams(torch, dev, E2E_SETS)
     h_logits = torch.from_numpy(inp["logits"]).pin_memory()
     h_x = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_y = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    h_y = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(E2E_SETS)]
 
     def run(n):
         st.fork()
         for i in range(n):
-            pool.step_host(h_logits, h_x, h_y[i & 1], None, rep_off, rep_ids, buf=i & 1, stream=st.s[i & 1])
+            b = i % E2E_SETS
+            pool.step_host(h_logits, h_x, h_y[b], None, rep_off, rep_ids, buf=b, stream=st.s[b])
         st.join()
 
-    run(4)
+    run(2 * E2E_SETS)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -451,13 +463,13 @@ def _e2e(a, w, inp, pool, rep_off, rep_ids, st, ws):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
     # the same layer run from device-resident inputs must give the same y
-    x = h_x.to(pool.workspace.device)
-    pool.plan(h_logits.to(pool.workspace.device), rep_off, rep_ids, buf=0)
+    x = h_x.to(dev)
+    pool.plan(h_logits.to(dev), rep_off, rep_ids, buf=0)
     pool.dispatch(x, buf=0)
     pool.identity_experts(w.T, buf=0)
     y = pool.combine(w.T, buf=0)
     torch.cuda.synchronize()
-    if not (torch.equal(h_y[0], y.cpu()) and torch.equal(h_y[1], y.cpu())):
+    if not all(torch.equal(h, y.cpu()) for h in h_y):
         raise RuntimeError("moe_step_host output differs from the device-resident path")
     if pool.check() != 0:
         raise RuntimeError("device error word set in the e2e pass")
