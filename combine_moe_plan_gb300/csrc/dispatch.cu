@@ -8,8 +8,9 @@
 //
 // GPU mapping: one warp per (token, 512-element segment).  Each lane loads 16
 // bf16 values (two 16-byte loads), a group of 128 elements spans 8 lanes, so
-// amax is a 3-step xor-shuffle; codes are rint((x * 127) / amax) with IEEE
-// fp32 division and round-half-even conversion; the lane's 16 codes leave as
+// amax is a 3-step xor-shuffle; codes are rint((x * 127) / amax), the
+// correctly rounded fp32 quotient (one reciprocal per group and Markstein's
+// correction per element) and round-half-even conversion; the lane's 16 codes leave as
 // one 16-byte store into each of the token's k rows; the 4 group scales of
 // the segment leave as one 16-byte store per row.  Reads of x are streamed
 // once; every byte of every destination row is written exactly once.
@@ -25,15 +26,38 @@ namespace {
 constexpr int kDispatchThreads = 256;  // 8 warps, 8 (token, segment) items per CTA
 constexpr int kSegElems = 512;         // 32 lanes x 16 elements
 
-__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float amax) {
-    // amax == 0 only when the whole group is +-0: dividing by 1 keeps codes 0.
-    const float den = amax > 0.0f ? amax : 1.0f;
-    const int qa = __float2int_rn((a * 127.0f) / den);
-    const int qb = __float2int_rn((b * 127.0f) / den);
-    const int qc = __float2int_rn((c * 127.0f) / den);
-    const int qd = __float2int_rn((d * 127.0f) / den);
-    return (uint32_t)(qa & 0xff) | ((uint32_t)(qb & 0xff) << 8) | ((uint32_t)(qc & 0xff) << 16) |
-           ((uint32_t)(qd & 0xff) << 24);
+// Correctly rounded binary32 quotient a / d for d > 0 with y = RN(1/d),
+// by Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): q0 = RN(a * y) is within one ulp of a/d, the residual a - d*q0 is
+// exact in one fma, and RN(q0 + r*y) is the correctly rounded quotient.
+// Valid while 1/d is a normal number and nothing overflows; the caller falls
+// back to the IEEE division otherwise.  Checked exhaustively against the
+// IEEE division over every bf16 activation and every bf16 significand of the
+// group maximum.
+__device__ __forceinline__ float div_rn(float a, float d, float y) {
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q0, d, a);
+    return __fmaf_rn(r, y, q0);
+}
+
+// Four codes rint((v * 127) / amax) packed little-endian into one word.
+template <bool FAST>
+__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float den, float inv) {
+    float qa, qb, qc, qd;
+    if (FAST) {
+        qa = div_rn(a * 127.0f, den, inv);
+        qb = div_rn(b * 127.0f, den, inv);
+        qc = div_rn(c * 127.0f, den, inv);
+        qd = div_rn(d * 127.0f, den, inv);
+    } else {
+        qa = (a * 127.0f) / den;
+        qb = (b * 127.0f) / den;
+        qc = (c * 127.0f) / den;
+        qd = (d * 127.0f) / den;
+    }
+    return (uint32_t)(__float2int_rn(qa) & 0xff) | ((uint32_t)(__float2int_rn(qb) & 0xff) << 8) |
+           ((uint32_t)(__float2int_rn(qc) & 0xff) << 16) | ((uint32_t)(__float2int_rn(qd) & 0xff) << 24);
 }
 
 __global__ void __launch_bounds__(kDispatchThreads)
@@ -79,11 +103,21 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
     MOE_TRACE_MARK(tr_dispatch, 1);
 
+    // amax == 0 only when the whole group is +-0: dividing by 1 keeps codes 0.
+    const float den = amax > 0.0f ? amax : 1.0f;
     uint4 q;
-    q.x = quant4(v[0], v[1], v[2], v[3], amax);
-    q.y = quant4(v[4], v[5], v[6], v[7], amax);
-    q.z = quant4(v[8], v[9], v[10], v[11], amax);
-    q.w = quant4(v[12], v[13], v[14], v[15], amax);
+    if (den >= 0x1p-126f && den <= 0x1p125f) {  // 1/den is a normal binary32
+        const float inv = __frcp_rn(den);
+        q.x = quant4<true>(v[0], v[1], v[2], v[3], den, inv);
+        q.y = quant4<true>(v[4], v[5], v[6], v[7], den, inv);
+        q.z = quant4<true>(v[8], v[9], v[10], v[11], den, inv);
+        q.w = quant4<true>(v[12], v[13], v[14], v[15], den, inv);
+    } else {
+        q.x = quant4<false>(v[0], v[1], v[2], v[3], den, 0.0f);
+        q.y = quant4<false>(v[4], v[5], v[6], v[7], den, 0.0f);
+        q.z = quant4<false>(v[8], v[9], v[10], v[11], den, 0.0f);
+        q.w = quant4<false>(v[12], v[13], v[14], v[15], den, 0.0f);
+    }
 
     const float scale = amax / 127.0f;
     float4 sc;

@@ -245,6 +245,7 @@ def test_quant_exhaustive_against_double_rounding_identity():
         for m in range(128):
             amaxes.append(np.float32((1.0 + m / 128.0) * 2.0 ** e))
     amaxes.append(np.float32(254.0))
+    amaxes += [wl.bf16_bits_to_f32(np.array([b], np.uint16))[0] for b in (0x0001, 0x0003, 0x0040, 0x007F)]
     rows = []
     for a in amaxes:
         xs = allx[np.abs(allx) <= a]
