@@ -282,3 +282,40 @@ def test_launch_count():
     Run(big, inp, pool=pool)
     assert pool.launches() - n0 == 6
     _check_all(big, inp, Run(big, inp, pool=pool))
+
+
+def test_step_captures_in_a_cuda_graph():
+    """plan -> dispatch -> combine (PDL launches) captured once in a CUDA graph
+    and replayed on new input contents gives the oracle's results."""
+    w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 512)
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
+    inp0 = wl.make_inputs(w, seed=0)
+    logits, x, ex = dev(inp0["logits"]), dev_bf16(inp0["x"]), dev_bf16(inp0["ex_out"])
+    ro, ri = dev(inp0["rep_off"]), dev(inp0["rep_ids"])
+    y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # warm
+        pool.plan(logits, ro, ri, buf=1, stream=s)
+        pool.dispatch(x, buf=1, stream=s)
+        pool.combine(w.T, y=y, ex_out=ex, buf=1, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pool.plan(logits, ro, ri, buf=1, stream=s)
+        pool.dispatch(x, buf=1, stream=s)
+        pool.combine(w.T, y=y, ex_out=ex, buf=1, stream=s)
+    for seed in (3, 4):
+        inp = wl.make_inputs(w, seed=seed)
+        logits.copy_(dev(inp["logits"]))
+        x.copy_(dev_bf16(inp["x"]))
+        ex.copy_(dev_bf16(inp["ex_out"]))
+        ro.copy_(dev(inp["rep_off"]))  # the replica map follows the seed's popularity ranking
+        ri.copy_(dev(inp["rep_ids"]))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.forward(inp["logits"], inp["x"], w.k, inp["rep_off"], inp["rep_ids"], w.P,
+                             ex_out=inp["ex_out"])
+        np.testing.assert_array_equal(pool.view(1)["slot"].cpu().numpy(), ref["slot"])
+        np.testing.assert_array_equal(pool.view(1)["codes"][:w.rows].cpu().numpy(), ref["codes"])
+        assert_y_close(host_u16(y), ref["y"], f"graph replay seed {seed}")
+    assert pool.check() == 0
