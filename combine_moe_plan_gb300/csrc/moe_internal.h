@@ -82,6 +82,6 @@ cudaError_t launch_combine(const uint16_t* ex_out, const int32_t* slot, const fl
 struct moe_pool {
     moe::Geometry geo;
     char* base;                       // device workspace
-    int32_t planned_T[moe::kMaxSets]; // T of the last moe_plan per set (0 = none)
+    int32_t planned_T[moe::kMaxSets]; // T of the last moe_plan per set (-1 = none)
     uint64_t launches;
 };

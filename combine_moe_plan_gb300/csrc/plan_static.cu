@@ -63,6 +63,15 @@ extern "C" MOE_API int moe_plan_static(const float* logits, int32_t T, int32_t E
                                        float* gates, int32_t* phys, int32_t* counts, int32_t* offsets,
                                        int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* error_word,
                                        void* stream) {
+    if (T == 0) {  // an empty batch: every expert window is empty
+        if (counts == nullptr || offsets == nullptr) return MOE_ERR_NULL;
+        if (P < 1 || P > 4096) return MOE_ERR_SIZE;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (cudaMemsetAsync(counts, 0, (size_t)P * sizeof(int32_t), s) != cudaSuccess ||
+            cudaMemsetAsync(offsets, 0, (size_t)(P + 1) * sizeof(int32_t), s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     if (logits == nullptr || topk_e == nullptr || gates == nullptr || phys == nullptr || counts == nullptr ||
         offsets == nullptr || slot == nullptr || src_token == nullptr || src_k == nullptr ||
         error_word == nullptr)

@@ -95,7 +95,7 @@ T* at(const moe_pool* p, size_t off) {
 int check_call(const moe_pool* pool, int32_t T, int buf) {
     if (pool == nullptr) return MOE_ERR_NULL;
     if (buf < 0 || buf >= pool->geo.d.n_sets) return MOE_ERR_BUF;
-    if (T < 1 || T > pool->geo.d.T_max) return MOE_ERR_SIZE;
+    if (T < 0 || T > pool->geo.d.T_max) return MOE_ERR_SIZE;
     return MOE_OK;
 }
 
@@ -126,6 +126,7 @@ MOE_API int moe_pool_init(const moe_desc* desc, void* dev_ws, size_t ws_bytes, m
     if (p == nullptr) return MOE_ERR_SIZE;
     p->geo = g;
     p->base = static_cast<char*>(dev_ws);
+    for (int b = 0; b < kMaxSets; ++b) p->planned_T[b] = -1;
     *out = p;
     return MOE_OK;
 }
@@ -199,14 +200,23 @@ MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T, const int32
                      const int32_t* rep_ids, int buf, void* stream) {
     int rc = check_call(pool, T, buf);
     if (rc != MOE_OK) return rc;
+    const moe_desc& d = pool->geo.d;
+    const SetLayout& L = pool->geo.set[buf];
+    pool->planned_T[buf] = -1;
+    if (T == 0) {  // an empty batch: every expert window is empty
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (cudaMemsetAsync(at<int32_t>(pool, L.counts), 0, (size_t)d.P * sizeof(int32_t), s) != cudaSuccess ||
+            cudaMemsetAsync(at<int32_t>(pool, L.offsets), 0, (size_t)(d.P + 1) * sizeof(int32_t), s) !=
+                cudaSuccess)
+            return MOE_ERR_CUDA;
+        pool->planned_T[buf] = 0;
+        return MOE_OK;
+    }
     if (logits == nullptr) return MOE_ERR_NULL;
     if (!aligned16(logits)) return MOE_ERR_ALIGN;
     if ((rep_off == nullptr) != (rep_ids == nullptr)) return MOE_ERR_NULL;
-    const moe_desc& d = pool->geo.d;
     if (rep_off == nullptr && d.P != d.E) return MOE_ERR_REPLICA;
     if (rep_off != nullptr && (!aligned16(rep_off) || !aligned16(rep_ids))) return MOE_ERR_ALIGN;
-    const SetLayout& L = pool->geo.set[buf];
-    pool->planned_T[buf] = 0;
     cudaError_t e = launch_plan(logits, T, d.E, d.P, d.k, rep_off, rep_ids, at<int32_t>(pool, L.topk_e),
                                 at<float>(pool, L.gates), at<int32_t>(pool, L.phys),
                                 at<int32_t>(pool, L.tile_hist), at<int32_t>(pool, L.local_rank),
@@ -223,9 +233,10 @@ MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T, const int32
 MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream) {
     int rc = check_call(pool, T, buf);
     if (rc != MOE_OK) return rc;
-    if (x == nullptr) return MOE_ERR_NULL;
-    if (!aligned16(x)) return MOE_ERR_ALIGN;
+    if (T > 0 && x == nullptr) return MOE_ERR_NULL;
+    if (T > 0 && !aligned16(x)) return MOE_ERR_ALIGN;
     if (pool->planned_T[buf] != T) return MOE_ERR_STATE;
+    if (T == 0) return MOE_OK;
     const moe_desc& d = pool->geo.d;
     const SetLayout& L = pool->geo.set[buf];
     return cuda_rc(launch_dispatch(x, T, d.H, d.k, at<int32_t>(pool, L.slot), at<int8_t>(pool, L.codes),
@@ -238,6 +249,7 @@ MOE_API int moe_identity_experts(moe_pool* pool, int32_t T, int buf, void* strea
     int rc = check_call(pool, T, buf);
     if (rc != MOE_OK) return rc;
     if (pool->planned_T[buf] != T) return MOE_ERR_STATE;
+    if (T == 0) return MOE_OK;
     const moe_desc& d = pool->geo.d;
     const SetLayout& L = pool->geo.set[buf];
     return cuda_rc(launch_identity_experts(at<int8_t>(pool, L.codes), at<float>(pool, L.scales), T * d.k, d.H,
@@ -248,9 +260,10 @@ MOE_API int moe_identity_experts(moe_pool* pool, int32_t T, int buf, void* strea
 MOE_API int moe_combine(moe_pool* pool, const uint16_t* ex_out, uint16_t* y, int32_t T, int buf, void* stream) {
     int rc = check_call(pool, T, buf);
     if (rc != MOE_OK) return rc;
-    if (y == nullptr) return MOE_ERR_NULL;
-    if (!aligned16(y) || (ex_out != nullptr && !aligned16(ex_out))) return MOE_ERR_ALIGN;
+    if (T > 0 && y == nullptr) return MOE_ERR_NULL;
+    if (T > 0 && (!aligned16(y) || (ex_out != nullptr && !aligned16(ex_out)))) return MOE_ERR_ALIGN;
     if (pool->planned_T[buf] != T) return MOE_ERR_STATE;
+    if (T == 0) return MOE_OK;
     const moe_desc& d = pool->geo.d;
     const SetLayout& L = pool->geo.set[buf];
     const uint16_t* src = ex_out != nullptr ? ex_out : at<uint16_t>(pool, L.ex_out);
@@ -264,6 +277,7 @@ MOE_API int moe_step_host(moe_pool* pool, const float* h_logits, const uint16_t*
                           void* stream) {
     int rc = check_call(pool, T, buf);
     if (rc != MOE_OK) return rc;
+    if (T == 0) return moe_plan(pool, h_logits, 0, rep_off, rep_ids, buf, stream);
     if (h_logits == nullptr || h_x == nullptr || h_y == nullptr) return MOE_ERR_NULL;
     const moe_desc& d = pool->geo.d;
     const SetLayout& L = pool->geo.set[buf];

@@ -169,7 +169,8 @@ MOE_API int moe_replica_check(const int32_t* rep_off, const int32_t* rep_ids, in
  * Then counts, offsets (exclusive scan, offsets[P] = T*k), slot[t,j] =
  * offsets[p] + (number of tokens before t routed to p), and the inverse
  * src_token / src_k.  Writes topk_e, gates, phys, counts, offsets, slot,
- * src_token, src_k of the set.  1 <= T <= T_max.
+ * src_token, src_k of the set.  0 <= T <= T_max; T = 0 (an empty batch)
+ * zeroes counts and offsets and launches no kernel (logits may be NULL).
  */
 MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T,
                      const int32_t* rep_off, const int32_t* rep_ids, int buf, void* stream);
@@ -180,7 +181,7 @@ MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T,
  * Per token and 128-element group g: amax = max |x|, scale = amax / 127 (fp32),
  * code = rint((x * 127) / amax) in fp32, half-even (amax = 0: scale 0, codes 0).
  * Row slot[t, j] of codes / scales receives token t's codes / scales for every
- * j.  Requires a prior moe_plan on this set with the same T.
+ * j.  Requires a prior moe_plan on this set with the same T (T = 0: no-op).
  */
 MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream);
 
@@ -197,7 +198,7 @@ MOE_API int moe_identity_experts(moe_pool* pool, int32_t T, int buf, void* strea
  *   ex_out  device bf16 [T*k (or more), H] expert outputs by row, or NULL to
  *           use the set's own ex_out buffer
  *   y       device bf16 [T, H] output
- * Requires a prior moe_plan on this set with the same T.
+ * Requires a prior moe_plan on this set with the same T (T = 0: no-op).
  */
 MOE_API int moe_combine(moe_pool* pool, const uint16_t* ex_out, uint16_t* y, int32_t T, int buf,
                         void* stream);

@@ -109,7 +109,7 @@ def test_calls_rejected_before_launch(L):
     good = ctypes.c_void_p(1 << 41)
     odd = ctypes.c_void_p((1 << 41) + 4)
     # T out of range, bad set, NULL and misaligned pointers
-    assert L.moe_plan(h, good, 0, None, None, 0, None) == -2
+    assert L.moe_plan(h, good, -1, None, None, 0, None) == -2
     assert L.moe_plan(h, good, 65, None, None, 0, None) == -2
     assert L.moe_plan(h, good, 8, None, None, 2, None) == -4
     assert L.moe_plan(h, None, 8, None, None, 0, None) == -1

@@ -319,3 +319,28 @@ def test_step_captures_in_a_cuda_graph():
         np.testing.assert_array_equal(pool.view(1)["codes"][:w.rows].cpu().numpy(), ref["codes"])
         assert_y_close(host_u16(y), ref["y"], f"graph replay seed {seed}")
     assert pool.check() == 0
+
+
+def test_empty_batch_and_maximum_sizes():
+    """T = 0 is a no-op with empty windows; P = 4096 (4 replicas per expert)
+    and H = 65536 go through the whole path."""
+    pool = moe.Pool(8, 256, 16, 16, 2)
+    v = pool.view(0)
+    v["counts"].fill_(7)
+    v["offsets"].fill_(7)
+    pool.plan(torch.empty((0, 16), dtype=torch.float32, device="cuda"))
+    pool.dispatch(torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"))
+    y = pool.combine(0)
+    assert y.shape == (0, 256) and pool.check() == 0
+    assert not v["counts"].any() and not v["offsets"].any()
+    ref = oracle.place(np.zeros((0, 2), np.int32), 16)
+    assert ref["offsets"].tolist() == [0] * 17
+    with pytest.raises(moe.MoeError):
+        pool.dispatch(torch.empty((1, 256), dtype=torch.bfloat16, device="cuda"))
+
+    rng = np.random.default_rng(10)
+    E, P = 1024, 4096
+    off = np.arange(0, P + 1, 4, dtype=np.int32)
+    ids = rng.permutation(P).astype(np.int32)
+    _custom(40, 128, E, P, 4, rng.standard_normal((40, E)), rep_off=off, rep_ids=ids)
+    _custom(6, 65536, 8, 8, 2, rng.standard_normal((6, 8)))
