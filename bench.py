@@ -228,8 +228,8 @@ class _Streams:
 
 def decode_latency(dev, reps=200):
     """Median GPU time of plan+dispatch (the routing metadata is part of the
-    fused dispatch) and of combine, each replayed as a CUDA graph, for the
-    96-token decode batch."""
+    fused dispatch) and of combine, each replayed as a CUDA graph, and of the
+    whole layer, for the 96-token decode batch."""
     import torch
     from combine_moe_plan_gb300 import moe
     w = wl.WORKLOADS["t96_h7168_e256_k8"]

@@ -84,13 +84,16 @@ __device__ __forceinline__ void lane_top2(const uint32_t (&key)[N], uint32_t& k1
     }
 }
 
+// Which kernel a route_tile call belongs to (its trace slice).
+constexpr int kRouteInRoute = 0, kRouteInSingle = 1;
+
 #ifdef MOE_TRACE
 // Stage stamps of route_tile go to the slice of the kernel that called it.
-template <bool SINGLE>
+template <int WHERE>
 __device__ __forceinline__ TraceSlice route_slice() {
-    return SINGLE ? tr_single_t : tr_route_t;
+    return WHERE == kRouteInRoute ? tr_route_t : tr_single_t;
 }
-#define ROUTE_MARK(stage) trace_mark(route_slice<SINGLE>(), (stage))
+#define ROUTE_MARK(stage) trace_mark(route_slice<WHERE>(), (stage))
 #else
 #define ROUTE_MARK(stage) ((void)0)
 #endif
@@ -101,6 +104,7 @@ constexpr int kRouteThreads = 32 * kTileTokens;  // one warp per token of the ti
 #ifndef MOE_PLAN_SINGLE_MAX_TILES
 #define MOE_PLAN_SINGLE_MAX_TILES 32
 #endif
+
 
 // Monotone map of finite floats onto uint32 (a < b  <=>  key(a) < key(b));
 // -0 is folded onto +0 first, so equal values give equal keys.  Every finite
@@ -114,7 +118,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // Route one 32-token tile (the body shared by both plan variants).
 // Trace stages: 0 start, 1 top-k done, 2 exp done, 3 sums done, 4 gates and
 // masks done, 5 tile counts and ranks written.
-template <int EPL, bool SINGLE>  // logits per lane = ceil(E / 32)
+template <int EPL, int WHERE>  // logits per lane = ceil(E / 32)
 __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int T, int E, int P, int k,
                                            const int32_t* __restrict__ rep_off,
                                            const int32_t* __restrict__ rep_ids, int32_t* __restrict__ topk_e,
@@ -280,8 +284,8 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     grid_dependency_sync();
     allow_dependents();
     MOE_TRACE_SM(tr_route);
-    route_tile<EPL, false>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles,
-                           local_rank, err, smem, blockIdx.x);
+    route_tile<EPL, kRouteInRoute>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
+                                   n_tiles, local_rank, err, smem, blockIdx.x);
 }
 
 // One warp: exclusive scan of tile_hist[p, :] in place, counts[p] = column
@@ -434,40 +438,17 @@ assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile
     src_k[r] = j;
 }
 
-// Single-launch plan for batches of at most MOE_PLAN_SINGLE_MAX_TILES tiles
-// (trace stages 0-5 as route_tile; the last CTA adds 6 scans done, 7 end)
-// (the decode regime): every CTA routes its tile; the CTA that finishes last
-// (atomic ticket, no waiting) then runs the column scans, the offsets and the
-// slot assignment for the whole batch, and resets the ticket for the next
-// call.  Each CTA fences its writes before taking its ticket, and the last
-// one reads the others' results with L1-bypassing loads.
-template <int EPL>
-__global__ void __launch_bounds__(kRouteThreads)
-plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
-                   const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
-                   int32_t* __restrict__ topk_e, float* __restrict__ gates, int32_t* __restrict__ phys,
-                   int32_t* __restrict__ tile_hist, int n_tiles, int32_t* __restrict__ local_rank,
-                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
-                   int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err,
-                   int32_t* __restrict__ ticket, int col_smem) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ int last;
-    grid_dependency_sync();
-    allow_dependents();
-    MOE_TRACE_SM(tr_single);
-    route_tile<EPL, true>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles,
-                          local_rank, err, smem, blockIdx.x);
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last = (atomicAdd(ticket, 1) == (int)gridDim.x - 1);
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-
-    // Column scans, one thread per expert (at most MOE_PLAN_SINGLE_MAX_TILES
-    // entries each): the loads of a column go out together, then a running
-    // sum.  Counts land in shared memory (scanned in place into offsets) and,
-    // when they fit (col_smem), so do the tile bases.
+// The single-launch tail, run by one CTA once every tile is routed: column
+// scans (one thread per expert; at most MOE_PLAN_SINGLE_MAX_TILES entries
+// each), offsets, and the placement of every (t, j) copy.  Counts land in
+// shared memory (scanned in place into offsets) and, when they fit
+// (col_smem), so do the tile bases.  Data written by other CTAs is read with
+// L1-bypassing loads.
+__device__ void plan_tail(int32_t* __restrict__ tile_hist, int n_tiles, int T, int P, int k,
+                          const int32_t* __restrict__ phys, const int32_t* __restrict__ local_rank,
+                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
+                          int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err,
+                          unsigned char* smem, int col_smem) {
     int32_t* offs = reinterpret_cast<int32_t*>(smem);  // [P+1], reuses the route scratch
     int32_t* colpre = offs + (P + 1);                   // [P, n_tiles] when col_smem
     for (int p = threadIdx.x; p < P; p += kRouteThreads) {
@@ -488,7 +469,6 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
         offs[p] = carry;
     }
     __syncthreads();
-    MOE_TRACE_MARK(tr_single, 6);
     block_scan_in_place<kRouteThreads>(offs, P);
     for (int q = threadIdx.x; q <= P; q += kRouteThreads) offsets[q] = offs[q];
     const int n = T * k;
@@ -511,11 +491,49 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
         src_token[r] = t;
         src_k[r] = j;
     }
+}
+
+// Single-launch plan for batches of at most MOE_PLAN_SINGLE_MAX_TILES tiles
+// (trace stages 0-5 as route_tile; the last CTA adds 6 scans done, 7 end)
+// (the decode regime): every CTA routes its tile; the CTA that finishes last
+// (atomic ticket, no waiting) then runs the column scans, the offsets and the
+// slot assignment for the whole batch, and resets the ticket for the next
+// call.  Each CTA fences its writes before taking its ticket, and the last
+// one reads the others' results with L1-bypassing loads.
+template <int EPL>
+__global__ void __launch_bounds__(kRouteThreads)
+plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
+                   const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
+                   int32_t* __restrict__ topk_e, float* __restrict__ gates, int32_t* __restrict__ phys,
+                   int32_t* __restrict__ tile_hist, int n_tiles, int32_t* __restrict__ local_rank,
+                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
+                   int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err,
+                   int32_t* __restrict__ ticket, int col_smem) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int last;
+    grid_dependency_sync();
+    allow_dependents();
+    MOE_TRACE_SM(tr_single);
+    route_tile<EPL, kRouteInSingle>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
+                                    n_tiles, local_rank, err, smem, blockIdx.x);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = (atomicAdd(ticket, 1) == (int)gridDim.x - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+
+    MOE_TRACE_MARK(tr_single, 6);
+    plan_tail(tile_hist, n_tiles, T, P, k, phys, local_rank, counts, offsets, slot, src_token, src_k, err, smem,
+              col_smem);
     if (threadIdx.x == 0) *ticket = 0;
     MOE_TRACE_MARK(tr_single, 7);
 }
 
+
 constexpr size_t kTailSmemMax = 96 * 1024;
+size_t tail_smem(size_t route_smem, int P, int n_tiles, int* col_smem);
+
 
 template <typename K>
 cudaError_t smem_attr(K kernel, size_t smem) {
@@ -532,12 +550,8 @@ cudaError_t launch_plan_epl(const float* logits, int T, int E, int P, int k, con
     const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
     cudaError_t e;
     if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
-        // The tail keeps offsets (P+1) and, when they fit, the tile bases
-        // (P x n_tiles) in shared memory.
-        const size_t tail = (size_t)(P + 1 + (size_t)P * n_tiles) * sizeof(int32_t);
-        const int col_smem = tail <= kTailSmemMax ? 1 : 0;
-        size_t need = col_smem ? tail : (size_t)(P + 1) * sizeof(int32_t);
-        const size_t smem1 = smem > need ? smem : need;
+        int col_smem = 0;
+        const size_t smem1 = tail_smem(smem, P, n_tiles, &col_smem);
         if ((e = smem_attr(plan_single_kernel<EPL>, smem1)) != cudaSuccess) return e;
         e = launch_pdl(plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem1, s, logits, T, E, P, k,
                        rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, counts, offsets,
@@ -565,6 +579,15 @@ cudaError_t launch_plan_epl(const float* logits, int T, int E, int P, int k, con
     return cudaSuccess;
 }
 
+// Shared memory for the single-launch tail: offsets and, when they fit, the
+// tile bases; returns the dynamic smem size and whether bases are in smem.
+size_t tail_smem(size_t route_smem, int P, int n_tiles, int* col_smem) {
+    const size_t tail = (size_t)(P + 1 + (size_t)P * n_tiles) * sizeof(int32_t);
+    *col_smem = tail <= kTailSmemMax ? 1 : 0;
+    const size_t need = *col_smem ? tail : (size_t)(P + 1) * sizeof(int32_t);
+    return route_smem > need ? route_smem : need;
+}
+
 }  // namespace
 
 #ifdef MOE_TRACE
@@ -587,6 +610,7 @@ int trace_symbols_plan(int kind, void** stamps, void** sms) {
             e = cudaGetSymbolAddress(stamps, tr_single_t);
             if (e == cudaSuccess) e = cudaGetSymbolAddress(sms, tr_single_sm);
             break;
+
         default:
             break;
     }

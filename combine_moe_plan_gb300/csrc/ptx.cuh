@@ -45,6 +45,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 __device__ __forceinline__ void set_error(int32_t* err, int bits) { atomicOr(err, bits); }
 
+
 // Programmatic dependent launch.  Every kernel of the library calls
 // grid_dependency_sync() before its first global-memory access: it returns once
 // the preceding kernel in the stream has completed and its writes are visible

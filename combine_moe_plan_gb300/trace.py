@@ -29,9 +29,9 @@ KINDS = {
     0: ("route_tile", ["start", "top-k", "exp", "sums", "gates+masks", "counts+ranks"]),
     1: ("column_scan", ["start", "end"]),
     2: ("assign", ["start", "offsets", "end"]),
-    3: ("plan_single", ["start", "top-k", "exp", "sums", "gates+masks", "counts+ranks", "scans(last)",
+    3: ("plan_single", ["start", "top-k", "exp", "sums", "gates+masks", "counts+ranks", "tail(last)",
                         "end(last)"]),
-    4: ("dispatch", ["start", "loaded", "quantized", "stored"]),
+    4: ("dispatch", ["start", "quantized", "slots", "stored"]),
     5: ("combine", ["start", "slots", "accumulated", "stored"]),
 }
 

@@ -40,7 +40,7 @@
  *     |x| >= 2^120) give unspecified values but no out-of-bounds access.
  *   - Kernels check every index they compute from data (replica map, slots);
  *     a bad one skips the access and sets a bit in the pool's device error
- *     word, read by moe_pool_check.  No kernel traps or spins without bound.
+ *     word, read by moe_pool_check.  No kernel traps or waits on a flag.
  */
 #ifndef MOE_H
 #define MOE_H
@@ -135,8 +135,8 @@ MOE_API int moe_pool_view(const moe_pool* pool, int buf, moe_view* view);
 
 /*
  * Zero the device error word and the pool's plan tickets (asynchronous on
- * `stream`).  Call once before the pool's first use, and never while the
- * pool's kernels run on another stream.
+ * `stream`).  Call once before the pool's first use, after any
+ * MOE_ERR_DEVICE, and never while the pool's kernels run on another stream.
  */
 MOE_API int moe_pool_clear_error(moe_pool* pool, void* stream);
 
