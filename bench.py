@@ -180,8 +180,8 @@ def run_reference(a, w: wl.Workload):
     t0 = time.perf_counter()
     run(0, 32)
     per_tok = (time.perf_counter() - t0) / 32
-    budget = 90.0  # seconds for warmup + timed steps
-    n_tok = int(max(1, min(w.T, budget / max(1, a.steps + a.warmup) / max(per_tok, 1e-9))))
+    budget = 90.0  # seconds for warmup + timed steps; at least 64 tokens per step
+    n_tok = int(max(min(64, w.T), min(w.T, budget / max(1, a.steps + a.warmup) / max(per_tok, 1e-9))))
     for _ in range(a.warmup):
         run(0, n_tok)
     t0 = time.perf_counter()

@@ -107,7 +107,10 @@ cudaError_t launch_identity_experts(const int8_t* codes, const float* scales, in
                                     uint16_t* ex_out, cudaStream_t s, uint64_t* launches) {
     const long long n = (long long)rows * (H / 16);
     long long blocks = (n + kExpertThreads - 1) / kExpertThreads;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    int dev = 0, sms = 1;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long cap = 16LL * (sms > 0 ? sms : 1);  // grid-stride: 16 CTAs of 256 per SM
+    if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     cudaError_t e = launch_pdl(identity_experts_kernel, dim3((unsigned)blocks), dim3(kExpertThreads), 0, s, codes,
                                scales, rows, H, Gs, ex_out);
