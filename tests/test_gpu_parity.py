@@ -344,3 +344,42 @@ def test_empty_batch_and_maximum_sizes():
     ids = rng.permutation(P).astype(np.int32)
     _custom(40, 128, E, P, 4, rng.standard_normal((40, E)), rep_off=off, rep_ids=ids)
     _custom(6, 65536, 8, 8, 2, rng.standard_normal((6, 8)))
+
+
+def test_bench_schedule_two_streams_full_size():
+    """The bench's timed schedule at the bench workload's full size: steps
+    alternate the two buffer sets on two streams, launched back to back, each
+    step with its own inputs and output buffer; every step's result is
+    checked against the oracle."""
+    w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    steps = []
+    for i in range(6):
+        inp = wl.make_inputs(w, seed=100 + i)
+        steps.append((inp, dev(inp["logits"]), dev_bf16(inp["x"]), dev_bf16(inp["ex_out"]),
+                      dev(inp["rep_off"]), dev(inp["rep_ids"]),
+                      torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")))
+    torch.cuda.synchronize()
+    ev = torch.cuda.Event()
+    ev.record()
+    for s in streams:
+        s.wait_event(ev)
+    for i, (_, logits, x, ex, ro, ri, y) in enumerate(steps):
+        s, b = streams[i & 1], i & 1
+        pool.plan(logits, ro, ri, buf=b, stream=s)
+        pool.dispatch(x, buf=b, stream=s)
+        pool.combine(w.T, y=y, ex_out=ex, buf=b, stream=s)
+    torch.cuda.synchronize()
+    assert pool.check() == 0
+    for i, (inp, *_, y) in enumerate(steps):
+        pl = oracle.plan(inp["logits"], w.k, inp["rep_off"], inp["rep_ids"], w.P)
+        assert_y_close(host_u16(y), oracle.combine(inp["ex_out"], pl["slot"], pl["gates"]), f"step {i}")
+    # the last step of each set left its plan and dispatch rows in the set
+    for i in (4, 5):
+        inp = steps[i][0]
+        v = pool.view(i & 1)
+        pl = oracle.plan(inp["logits"], w.k, inp["rep_off"], inp["rep_ids"], w.P)
+        np.testing.assert_array_equal(v["slot"].cpu().numpy(), pl["slot"])
+        codes, _ = oracle.dispatch(inp["x"], pl["slot"])
+        np.testing.assert_array_equal(v["codes"][:w.rows].cpu().numpy(), codes)
