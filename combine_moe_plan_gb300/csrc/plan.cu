@@ -9,8 +9,9 @@
 //
 // Three launches for large batches (one for small ones, see plan_single_kernel):
 //   route_tile   one CTA of 32 warps per tile of 32 tokens, one warp per
-//                token: k rounds of shuffle arg-max (ties -> lower expert
-//                id).  The CTA then computes the gates in fp64 with one
+//                token: k rounds of warp arg-max by redux.sync over each
+//                lane's cached two largest keys (ties -> lower expert id).
+//                The CTA then computes the gates in fp64 with one
 //                (token, j) pair per thread, applies the replica map, and sets
 //                bit t of a shared-memory mask per physical expert.  From the
 //                mask: the tile's count per expert (popc) and each copy's rank
@@ -37,30 +38,6 @@ MOE_TRACE_BUFFERS(tr_assign)
 
 namespace moe {
 namespace {
-
-// Largest key of a lane and its slot r (the lowest r among equal keys): a
-// tree over adjacent pairs, so the left (lower-r) side wins ties.
-template <int N>
-__device__ __forceinline__ void lane_max(const uint32_t (&key)[N], uint32_t& m, int& r) {
-    uint32_t v[N];
-    int id[N];
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        v[i] = key[i];
-        id[i] = i;
-    }
-#pragma unroll
-    for (int w = N / 2; w >= 1; w /= 2) {
-#pragma unroll
-        for (int i = 0; i < w; ++i) {
-            const bool take = v[2 * i + 1] > v[2 * i];
-            v[i] = take ? v[2 * i + 1] : v[2 * i];
-            id[i] = take ? id[2 * i + 1] : id[2 * i];
-        }
-    }
-    m = v[0];
-    r = id[0];
-}
 
 // The two largest keys of a lane and their slots (lower slot first among
 // equal keys); k2 = 0 if the lane has fewer than two keys above 0.
