@@ -143,6 +143,19 @@ def max_over_ranks(vals, device=None):
     return t.tolist()
 
 
+def _percentiles_us(ms_list) -> list:
+    """p10, median and p90 of a list of event times in ms, in microseconds."""
+    v = np.sort(np.asarray(ms_list, np.float64)) * 1e3
+    return [float(np.percentile(v, q)) for q in (10, 50, 90)]
+
+
+def _host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def _oracle_step_fn(w: wl.Workload, inp: dict):
     """A function running the oracle over tokens [a, b) of the workload."""
     import oracle
@@ -154,21 +167,39 @@ def _oracle_step_fn(w: wl.Workload, inp: dict):
     return run
 
 
-def cpu_baseline(w: wl.Workload, inp: dict, budget_s: float = 15.0) -> dict:
-    """The oracle as it stands on one host core, on a bounded sample of the
-    workload: whole batches while they fit the budget, else a token prefix."""
-    run = _oracle_step_fn(w, inp)
+def _oracle_threads(n: int) -> int:
+    import oracle
+    return oracle.set_threads(n)
+
+
+def _time_oracle(run, T: int, budget_s: float, max_reps: int):
+    """Whole batches while they fit the budget, else a token prefix."""
     t0 = time.perf_counter()
-    run(0, min(w.T, 64))
-    per_tok = (time.perf_counter() - t0) / min(w.T, 64)
-    n_tok = int(max(64, min(w.T, budget_s / max(per_tok, 1e-9))))
-    reps = max(1, min(30, int(budget_s / (per_tok * n_tok))))
+    run(0, min(T, 64))
+    per_tok = (time.perf_counter() - t0) / min(T, 64)
+    n_tok = int(max(min(T, 64), min(T, budget_s / max(per_tok, 1e-9))))
+    reps = max(1, min(max_reps, int(budget_s / (per_tok * n_tok))))
     t0 = time.perf_counter()
     for _ in range(reps):
         run(0, n_tok)
-    dt = time.perf_counter() - t0
-    return {"value": reps * n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x the first {n_tok} tokens of {w.name} (plan+dispatch+combine, single thread)"}
+    return reps, n_tok, time.perf_counter() - t0
+
+
+def cpu_baseline(w: wl.Workload, inp: dict, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload: once with its per-token loops on every core (the reported
+    value), once on a single thread.  The outputs of the two are identical."""
+    run = _oracle_step_fn(w, inp)
+    n_thr = _oracle_threads(_host_cores())
+    reps, n_tok, dt = _time_oracle(run, w.T, budget_s, 200)
+    _oracle_threads(1)
+    reps1, n_tok1, dt1 = _time_oracle(run, w.T, budget_s, 30)
+    _oracle_threads(n_thr)
+    return {"value": reps * n_tok / dt, "unit": "tokens/s", "cores": n_thr, "kind": "oracle",
+            "sample": f"{reps} x the first {n_tok} tokens of {w.name} (plan+dispatch+combine, "
+                      f"per-token loops on {n_thr} threads, counting sort serial)",
+            "single_thread": {"value": reps1 * n_tok1 / dt1, "cores": 1,
+                              "sample": f"{reps1} x the first {n_tok1} tokens"}}
 
 
 def run_reference(a, w: wl.Workload):
@@ -177,9 +208,10 @@ def run_reference(a, w: wl.Workload):
         return
     inp = wl.make_inputs(w)
     run = _oracle_step_fn(w, inp)
+    n_thr = _oracle_threads(_host_cores())
     t0 = time.perf_counter()
-    run(0, 32)
-    per_tok = (time.perf_counter() - t0) / 32
+    run(0, 64)
+    per_tok = (time.perf_counter() - t0) / 64
     budget = 90.0  # seconds for warmup + timed steps; at least 64 tokens per step
     n_tok = int(max(min(64, w.T), min(w.T, budget / max(1, a.steps + a.warmup) / max(per_tok, 1e-9))))
     for _ in range(a.warmup):
@@ -189,14 +221,15 @@ def run_reference(a, w: wl.Workload):
         run(0, n_tok)
     dt = time.perf_counter() - t0
     v = a.steps * n_tok / dt
-    sample = f"first {n_tok} tokens of {w.name} per step (plan+dispatch+combine, single thread)"
+    sample = (f"first {n_tok} tokens of {w.name} per step (plan+dispatch+combine, "
+              f"per-token loops on {n_thr} threads)")
     print(json.dumps({
         "impl": "reference", "metric": "dispatch+combine tokens/s (plan+dispatch+combine per step)",
         "value": v, "unit": "tokens/s", "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8+bf16", "data": "synthetic",
         "config": {"workload": w.name, "tokens_per_step": n_tok, "H": w.H, "E": w.E, "P": w.P, "k": w.k},
-        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": n_thr, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -227,9 +260,9 @@ class _Streams:
 
 
 def decode_latency(dev, reps=200):
-    """Median GPU time of plan+dispatch (the routing metadata is part of the
-    fused dispatch) and of combine, each replayed as a CUDA graph, and of the
-    whole layer, for the 96-token decode batch."""
+    """GPU time (median, with p10 and p90) of plan+dispatch (the routing
+    metadata is part of the fused dispatch) and of combine, each replayed as
+    a CUDA graph, and of the whole layer, for the 96-token decode batch."""
     import torch
     from combine_moe_plan_gb300 import moe
     w = wl.WORKLOADS["t96_h7168_e256_k8"]
@@ -267,11 +300,12 @@ def decode_latency(dev, reps=200):
             fn()
             e1.record()
             e1.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e3)
-        return statistics.median(ts)
+            ts.append(e0.elapsed_time(e1))
+        return _percentiles_us(ts)
 
-    out = {"workload": w.name, "dispatch_us": med(g_disp.replay), "combine_us": med(g_comb.replay),
-           "layer_us": med(g_layer.replay),
+    pct = {"dispatch": med(g_disp.replay), "combine": med(g_comb.replay), "layer": med(g_layer.replay)}
+    out = {"workload": w.name, "dispatch_us": pct["dispatch"][1], "combine_us": pct["combine"][1],
+           "layer_us": pct["layer"][1], "p10_p50_p90_us": pct,
            "note": "CUDA-graph replays from an idle GPU; dispatch = plan + dispatch (the fused "
                    "dispatch carries the routing metadata); each graph launch adds its own overhead"}
     if pool.check() != 0:
@@ -348,6 +382,7 @@ def run_ours(a, w: wl.Workload):
         per["combine"].append(e[2].elapsed_time(e[3]))
         per["step"].append(e[0].elapsed_time(e[3]))
     per_us = {k: 1e3 * statistics.median(v) for k, v in per.items()}
+    per_pct = {k: _percentiles_us(v) for k, v in per.items()}
     mean_us = {k: 1e3 * statistics.fmean(v) for k, v in per.items()}
 
     # ---- phase B (timed region): K steps, the two buffer sets on two streams ----
@@ -404,6 +439,8 @@ def run_ours(a, w: wl.Workload):
             "us_per_call": {"plan": per_us["plan"], "dispatch": per_us["dispatch"],
                             "combine": per_us["combine"], "step_serialized": per_us["step"],
                             "step_pipelined": ms * 1e3},
+            "us_per_call_p10_p50_p90": {"plan": per_pct["plan"], "dispatch": per_pct["dispatch"],
+                                        "combine": per_pct["combine"], "step_serialized": per_pct["step"]},
             "hbm_gbs": {"step": bytes_["total"] / (ms * 1e-3) / 1e9,
                         "step_serialized": bytes_["total"] / (per_us["step"] * 1e-6) / 1e9,
                         "dispatch": bytes_["dispatch"] / (per_us["dispatch"] * 1e-6) / 1e9,

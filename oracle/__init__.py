@@ -36,14 +36,18 @@ class OracleError(RuntimeError):
     pass
 
 
+_FLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
 def build(force: bool = False) -> str:
-    """Compile moe_oracle.c into a shared library (gcc, ISO C11, no FP contraction)."""
+    """Compile moe_oracle.c into a shared library (gcc, ISO C11, no FP
+    contraction), with OpenMP for the per-token loops where gcc has it."""
     os.makedirs(_LIBDIR, exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-               "-shared", "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
+        r = subprocess.run(["gcc", *_FLAGS, "-fopenmp", "-o", tmp, _SRC, "-lm"], capture_output=True)
+        if r.returncode != 0:  # no OpenMP runtime: the same loops, serial
+            subprocess.run(["gcc", *_FLAGS, "-o", tmp, _SRC, "-lm"], check=True)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -64,12 +68,24 @@ def _load():
             lib.orc_combine.argtypes = [P, i32, i32, i32, P, P, i32, P]
             lib.orc_combine_tokens.argtypes = [P, i32, i32, i32, P, P, P, i32, P]
             lib.orc_f32_to_bf16_array.argtypes = [P, ctypes.c_int64, P]
+            lib.orc_set_threads.argtypes = [ctypes.c_int]
+            lib.orc_set_threads.restype = ctypes.c_int
             for f in ("orc_route", "orc_place", "orc_quantize", "orc_dispatch",
                       "orc_identity_experts", "orc_combine", "orc_combine_tokens"):
                 getattr(lib, f).restype = ctypes.c_int
             lib.orc_f32_to_bf16_array.restype = None
             _lib = lib
     return _lib
+
+
+def set_threads(n: int = 0) -> int:
+    """Threads for the per-token loops (n < 1: keep the current setting).
+    Returns the count now in force (1 when built without OpenMP)."""
+    return int(_load().orc_set_threads(int(n)))
+
+
+def threads() -> int:
+    return set_threads(0)
 
 
 def _p(a):

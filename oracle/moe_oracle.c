@@ -32,18 +32,51 @@
  *
  * Plain loops, one step after another, no blocking or fusion.  Every function
  * returns 0 on success or a negative code for inputs outside the method's
- * domain.  Build: gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared -lm.
+ * domain (outputs are then unspecified).  Build: gcc -std=c11 -O2
+ * -ffp-contract=off -fPIC -shared -lm, plus -fopenmp where the compiler has
+ * it: the per-token loops (route, quantize, dispatch, experts, combine) then
+ * split their tokens over threads.  Each token's arithmetic is the same in
+ * either build, so the results are identical; the counting sort stays serial.
+ * When several tokens are bad, the lowest token's error code is returned, as
+ * a serial loop would.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_OK 0
 #define ORC_ERR_ARG (-1)
 #define ORC_ERR_REPLICA (-2)
 #define ORC_ERR_DUPLICATE (-3)
 #define ORC_ERR_NONFINITE (-4)
+
+/* ------------------------------------------------------------ threads ---- */
+
+/* Threads the per-token loops use (1 without OpenMP).  n < 1 leaves it as is. */
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
+/* Record a failing token; the lowest token index keeps its code. */
+static void orc_note_error(int32_t t, int rc, int32_t* err_t, int* err_rc) {
+#pragma omp critical(orc_error)
+    {
+        if (*err_t < 0 || t < *err_t) {
+            *err_t = t;
+            *err_rc = rc;
+        }
+    }
+}
 
 /* ---------------------------------------------------------------- bf16 ---- */
 
@@ -93,47 +126,61 @@ static int orc_cand_cmp(const void* pa, const void* pb) {
  * in fp64, ascending j; gate_j = (float)(e_j / s).
  * Replica: the token at index t picks replica t mod (replica count).
  */
+static int orc_route_token(const float* row, int32_t t, int32_t E, int32_t k,
+                           const int32_t* rep_off, const int32_t* rep_ids, int32_t P,
+                           orc_cand* c, double* ex,
+                           int32_t* topk_e, float* gates, int32_t* phys) {
+    for (int32_t e = 0; e < E; ++e) {
+        if (!isfinite(row[e])) return ORC_ERR_NONFINITE;
+        c[e].v = row[e];
+        c[e].e = e;
+    }
+    qsort(c, (size_t)E, sizeof(orc_cand), orc_cand_cmp);
+
+    double s = 0.0;
+    for (int32_t j = 0; j < k; ++j) {
+        ex[j] = exp((double)c[j].v - (double)c[0].v);
+        s += ex[j];
+    }
+    for (int32_t j = 0; j < k; ++j) {
+        int32_t e = c[j].e;
+        int32_t p = e;
+        if (rep_off) {
+            int32_t lo = rep_off[e], n = rep_off[e + 1] - rep_off[e];
+            if (n < 1 || lo < 0 || lo + n > P) return ORC_ERR_REPLICA;
+            p = rep_ids[lo + (t % n)];
+            if (p < 0 || p >= P) return ORC_ERR_REPLICA;
+        }
+        topk_e[j] = e;
+        gates[j] = (float)(ex[j] / s);
+        phys[j] = p;
+    }
+    return ORC_OK;
+}
+
 int orc_route(const float* logits, int32_t T, int32_t E, int32_t k,
               const int32_t* rep_off, const int32_t* rep_ids, int32_t P,
               int32_t* topk_e, float* gates, int32_t* phys) {
     if (!logits || !topk_e || !gates || !phys || T < 0 || E < 1 || k < 1 || k > E || P < E)
         return ORC_ERR_ARG;
-    orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)E);
-    double* ex = (double*)malloc(sizeof(double) * (size_t)k);
-    if (!c || !ex) { free(c); free(ex); return ORC_ERR_ARG; }
-    int rc = ORC_OK;
-    for (int32_t t = 0; t < T && rc == ORC_OK; ++t) {
-        const float* row = logits + (size_t)t * E;
-        for (int32_t e = 0; e < E; ++e) {
-            if (!isfinite(row[e])) { rc = ORC_ERR_NONFINITE; break; }
-            c[e].v = row[e];
-            c[e].e = e;
+    int32_t err_t = -1;
+    int err_rc = ORC_OK;
+#pragma omp parallel
+    {
+        orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)E);
+        double* ex = (double*)malloc(sizeof(double) * (size_t)k);
+#pragma omp for schedule(static)
+        for (int32_t t = 0; t < T; ++t) {
+            int rc = (c && ex) ? orc_route_token(logits + (size_t)t * E, t, E, k, rep_off, rep_ids, P, c, ex,
+                                                 topk_e + (size_t)t * k, gates + (size_t)t * k,
+                                                 phys + (size_t)t * k)
+                               : ORC_ERR_ARG;
+            if (rc != ORC_OK) orc_note_error(t, rc, &err_t, &err_rc);
         }
-        if (rc != ORC_OK) break;
-        qsort(c, (size_t)E, sizeof(orc_cand), orc_cand_cmp);
-
-        double s = 0.0;
-        for (int32_t j = 0; j < k; ++j) {
-            ex[j] = exp((double)c[j].v - (double)c[0].v);
-            s += ex[j];
-        }
-        for (int32_t j = 0; j < k; ++j) {
-            int32_t e = c[j].e;
-            int32_t p = e;
-            if (rep_off) {
-                int32_t lo = rep_off[e], n = rep_off[e + 1] - rep_off[e];
-                if (n < 1 || lo < 0 || lo + n > P) { rc = ORC_ERR_REPLICA; break; }
-                p = rep_ids[lo + (t % n)];
-                if (p < 0 || p >= P) { rc = ORC_ERR_REPLICA; break; }
-            }
-            topk_e[(size_t)t * k + j] = e;
-            gates[(size_t)t * k + j] = (float)(ex[j] / s);
-            phys[(size_t)t * k + j] = p;
-        }
+        free(c);
+        free(ex);
     }
-    free(c);
-    free(ex);
-    return rc;
+    return err_rc;
 }
 
 /* ------------------------------------------------------ placement (a4-a6) */
@@ -194,34 +241,44 @@ int orc_place(const int32_t* phys, int32_t T, int32_t k, int32_t P,
  * code = rint((x * 127) / amax) in fp32, round-half-even; amax == 0 gives
  * scale 0 and all-zero codes.  |x| <= amax makes |code| <= 127.
  */
+static int orc_quantize_token(const uint16_t* x, int32_t H, int8_t* codes, float* scales) {
+    const int32_t G = H / 128;
+    for (int32_t g = 0; g < G; ++g) {
+        const uint16_t* xs = x + (size_t)g * 128;
+        float amax = 0.0f;
+        for (int32_t i = 0; i < 128; ++i) {
+            float v = orc_bf16_to_f32(xs[i]);
+            if (!isfinite(v)) return ORC_ERR_NONFINITE;
+            float a = fabsf(v);
+            if (a > amax) amax = a;
+        }
+        scales[g] = amax / 127.0f;
+        for (int32_t i = 0; i < 128; ++i) {
+            int8_t q = 0;
+            if (amax > 0.0f) {
+                float v = orc_bf16_to_f32(xs[i]);
+                float num = v * 127.0f;
+                float quo = num / amax;
+                q = (int8_t)(int32_t)rintf(quo);
+            }
+            codes[(size_t)g * 128 + i] = q;
+        }
+    }
+    return ORC_OK;
+}
+
 int orc_quantize(const uint16_t* x, int32_t T, int32_t H,
                  int8_t* codes, float* scales) {
     if (!x || !codes || !scales || T < 0 || H < 128 || H % 128 != 0) return ORC_ERR_ARG;
     const int32_t G = H / 128;
+    int32_t err_t = -1;
+    int err_rc = ORC_OK;
+#pragma omp parallel for schedule(static)
     for (int32_t t = 0; t < T; ++t) {
-        for (int32_t g = 0; g < G; ++g) {
-            const uint16_t* xs = x + (size_t)t * H + (size_t)g * 128;
-            float amax = 0.0f;
-            for (int32_t i = 0; i < 128; ++i) {
-                float v = orc_bf16_to_f32(xs[i]);
-                if (!isfinite(v)) return ORC_ERR_NONFINITE;
-                float a = fabsf(v);
-                if (a > amax) amax = a;
-            }
-            scales[(size_t)t * G + g] = amax / 127.0f;
-            for (int32_t i = 0; i < 128; ++i) {
-                int8_t q = 0;
-                if (amax > 0.0f) {
-                    float v = orc_bf16_to_f32(xs[i]);
-                    float num = v * 127.0f;
-                    float quo = num / amax;
-                    q = (int8_t)(int32_t)rintf(quo);
-                }
-                codes[(size_t)t * H + (size_t)g * 128 + i] = q;
-            }
-        }
+        int rc = orc_quantize_token(x + (size_t)t * H, H, codes + (size_t)t * H, scales + (size_t)t * G);
+        if (rc != ORC_OK) orc_note_error(t, rc, &err_t, &err_rc);
     }
-    return ORC_OK;
+    return err_rc;
 }
 
 /*
@@ -237,22 +294,27 @@ int orc_dispatch(const uint16_t* x, int32_t T, int32_t H, int32_t k,
     if (!x || !slot || !pool_codes || !pool_scales || T < 0 || k < 1 || H < 128 || H % 128 != 0)
         return ORC_ERR_ARG;
     const int32_t G = H / 128;
-    int8_t* codes = (int8_t*)malloc((size_t)H);
-    float* scales = (float*)malloc(sizeof(float) * (size_t)G);
-    if (!codes || !scales) { free(codes); free(scales); return ORC_ERR_ARG; }
-    int rc = ORC_OK;
-    for (int32_t t = 0; t < T && rc == ORC_OK; ++t) {
-        rc = orc_quantize(x + (size_t)t * H, 1, H, codes, scales);
-        for (int32_t j = 0; j < k && rc == ORC_OK; ++j) {
-            int32_t r = slot[(size_t)t * k + j];
-            if (r < 0 || r >= R) { rc = ORC_ERR_ARG; break; }
-            memcpy(pool_codes + (size_t)r * H, codes, (size_t)H);
-            memcpy(pool_scales + (size_t)r * G, scales, sizeof(float) * (size_t)G);
+    int32_t err_t = -1;
+    int err_rc = ORC_OK;
+#pragma omp parallel
+    {
+        int8_t* codes = (int8_t*)malloc((size_t)H);
+        float* scales = (float*)malloc(sizeof(float) * (size_t)G);
+#pragma omp for schedule(static)
+        for (int32_t t = 0; t < T; ++t) {
+            int rc = (codes && scales) ? orc_quantize_token(x + (size_t)t * H, H, codes, scales) : ORC_ERR_ARG;
+            for (int32_t j = 0; j < k && rc == ORC_OK; ++j) {
+                int32_t r = slot[(size_t)t * k + j];
+                if (r < 0 || r >= R) { rc = ORC_ERR_ARG; break; }
+                memcpy(pool_codes + (size_t)r * H, codes, (size_t)H);
+                memcpy(pool_scales + (size_t)r * G, scales, sizeof(float) * (size_t)G);
+            }
+            if (rc != ORC_OK) orc_note_error(t, rc, &err_t, &err_rc);
         }
+        free(codes);
+        free(scales);
     }
-    free(codes);
-    free(scales);
-    return rc;
+    return err_rc;
 }
 
 /* --------------------------------------------------------- experts (a9) -- */
@@ -262,6 +324,7 @@ int orc_identity_experts(const int8_t* codes, const float* scales, int32_t rows,
                          uint16_t* out) {
     if (!codes || !scales || !out || rows < 0 || H < 128 || H % 128 != 0) return ORC_ERR_ARG;
     const int32_t G = H / 128;
+#pragma omp parallel for schedule(static)
     for (int32_t r = 0; r < rows; ++r)
         for (int32_t i = 0; i < H; ++i) {
             float v = (float)codes[(size_t)r * H + i] * scales[(size_t)r * G + i / 128];
@@ -280,24 +343,33 @@ int orc_identity_experts(const int8_t* codes, const float* scales, int32_t rows,
  * acc = 0; for j = 0..k-1: acc = fmaf(gate_j, ex_out[slot_j, i], acc);
  * y = bf16(acc).
  */
+static int orc_combine_token(const uint16_t* ex_out, int32_t R, int32_t H, int32_t k,
+                             const int32_t* slot, const float* gates, uint16_t* y) {
+    for (int32_t j = 0; j < k; ++j) {
+        int32_t r = slot[j];
+        if (r < 0 || r >= R) return ORC_ERR_ARG;
+    }
+    for (int32_t i = 0; i < H; ++i) {
+        float acc = 0.0f;
+        for (int32_t j = 0; j < k; ++j)
+            acc = fmaf(gates[j], orc_bf16_to_f32(ex_out[(size_t)slot[j] * H + i]), acc);
+        y[i] = orc_f32_to_bf16(acc);
+    }
+    return ORC_OK;
+}
+
 int orc_combine(const uint16_t* ex_out, int32_t R, int32_t H, int32_t k,
                 const int32_t* slot, const float* gates, int32_t T, uint16_t* y) {
     if (!ex_out || !slot || !gates || !y || T < 0 || k < 1 || H < 1) return ORC_ERR_ARG;
+    int32_t err_t = -1;
+    int err_rc = ORC_OK;
+#pragma omp parallel for schedule(static)
     for (int32_t t = 0; t < T; ++t) {
-        for (int32_t j = 0; j < k; ++j) {
-            int32_t r = slot[(size_t)t * k + j];
-            if (r < 0 || r >= R) return ORC_ERR_ARG;
-        }
-        for (int32_t i = 0; i < H; ++i) {
-            float acc = 0.0f;
-            for (int32_t j = 0; j < k; ++j) {
-                int32_t r = slot[(size_t)t * k + j];
-                acc = fmaf(gates[(size_t)t * k + j], orc_bf16_to_f32(ex_out[(size_t)r * H + i]), acc);
-            }
-            y[(size_t)t * H + i] = orc_f32_to_bf16(acc);
-        }
+        int rc = orc_combine_token(ex_out, R, H, k, slot + (size_t)t * k, gates + (size_t)t * k,
+                                   y + (size_t)t * H);
+        if (rc != ORC_OK) orc_note_error(t, rc, &err_t, &err_rc);
     }
-    return ORC_OK;
+    return err_rc;
 }
 
 /*
@@ -308,14 +380,17 @@ int orc_combine(const uint16_t* ex_out, int32_t R, int32_t H, int32_t k,
 int orc_combine_tokens(const uint16_t* ex_out, int32_t R, int32_t H, int32_t k,
                        const int32_t* slot, const float* gates,
                        const int32_t* tok, int32_t n, uint16_t* y_sub) {
-    if (!tok || n < 0) return ORC_ERR_ARG;
+    if (!ex_out || !slot || !gates || !tok || !y_sub || n < 0 || k < 1 || H < 1) return ORC_ERR_ARG;
+    int32_t err_s = -1;
+    int err_rc = ORC_OK;
+#pragma omp parallel for schedule(static)
     for (int32_t s = 0; s < n; ++s) {
         int32_t t = tok[s];
-        int rc = orc_combine(ex_out, R, H, k, slot + (size_t)t * k, gates + (size_t)t * k, 1,
-                             y_sub + (size_t)s * H);
-        if (rc != ORC_OK) return rc;
+        int rc = orc_combine_token(ex_out, R, H, k, slot + (size_t)t * k, gates + (size_t)t * k,
+                                   y_sub + (size_t)s * H);
+        if (rc != ORC_OK) orc_note_error(s, rc, &err_s, &err_rc);
     }
-    return ORC_OK;
+    return err_rc;
 }
 
 /* bf16 helpers exposed for the oracle's own pin tests. */

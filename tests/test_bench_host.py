@@ -68,5 +68,18 @@ def test_reference_arm_rank0_only():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "t64_h256_e8_k2"
+
+
+def test_cpu_baseline_reports_all_cores_and_single_thread():
+    import bench
+    import oracle
+    from combine_moe_plan_gb300 import workloads as wl
+    before = oracle.threads()
+    w = wl.WORKLOADS["t64_h256_e8_k2"]
+    d = bench.cpu_baseline(w, wl.make_inputs(w), budget_s=0.2)
+    assert d["kind"] == "oracle" and d["value"] > 0 and d["unit"] == "tokens/s"
+    assert d["cores"] == oracle.threads() >= 1
+    assert d["single_thread"]["cores"] == 1 and d["single_thread"]["value"] > 0
+    oracle.set_threads(before)
