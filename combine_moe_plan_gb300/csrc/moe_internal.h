@@ -39,20 +39,44 @@ int make_geometry(const moe_desc* d, Geometry* g);
 // Launch with programmatic stream serialization, so that the kernel can be
 // scheduled while the previous kernel in the stream drains (the kernel itself
 // waits for it in grid_dependency_sync before touching global memory).
+// `priority` != 0 adds a launch priority (cudaLaunchAttributePriority; lower
+// numbers are more urgent).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       Args... args) {
+cudaError_t launch_pdl_at(int priority, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributePriority;
+    attr[1].val.priority = priority;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = priority != 0 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+    return launch_pdl_at(0, kernel, grid, block, smem, s, args...);
+}
+
+// The most urgent launch priority the device offers (cudaDeviceGetStreamPriorityRange's
+// "greatest" value; 0 where the device has no priorities).  Looked up once.
+inline int most_urgent_priority() {
+    static const int v = [] {
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        return greatest;
+    }();
+    return v;
 }
 
 // Launchers: enqueue on `s`, return cudaGetLastError() after the launch(es).

@@ -530,32 +530,39 @@ cudaError_t launch_plan_epl(const float* logits, int T, int E, int P, int k, con
                             int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err, int32_t* ticket,
                             size_t smem, cudaStream_t s, uint64_t* launches) {
     const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
+    // The plan is latency-bound and on its stream's critical path; bandwidth-
+    // bound kernels of other streams (the other buffer set's dispatch and
+    // combine) keep HBM busy meanwhile.  At the most urgent priority the block
+    // scheduler places the plan's CTAs ahead of their queued CTAs, so the plan
+    // is not stretched by waiting for SM slots.
+    const int urgent = most_urgent_priority();
     cudaError_t e;
     if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
         int col_smem = 0;
         const size_t smem1 = tail_smem(smem, P, n_tiles, &col_smem);
         if ((e = smem_attr(plan_single_kernel<EPL>, smem1)) != cudaSuccess) return e;
-        e = launch_pdl(plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem1, s, logits, T, E, P, k,
-                       rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, counts, offsets,
-                       slot, src_token, src_k, err, ticket, col_smem);
+        e = launch_pdl_at(urgent, plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem1, s, logits,
+                          T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank,
+                          counts, offsets, slot, src_token, src_k, err, ticket, col_smem);
         if (e == cudaSuccess) *launches += 1;
         return e;
     }
     if ((e = smem_attr(route_tile_kernel<EPL>, smem)) != cudaSuccess) return e;
-    e = launch_pdl(route_tile_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem, s, logits, T, E, P, k,
-                   rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, err);
+    e = launch_pdl_at(urgent, route_tile_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem, s, logits, T, E,
+                      P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, err);
     if (e != cudaSuccess) return e;
     *launches += 1;
 
-    e = launch_pdl(column_scan_kernel, dim3((P + 7) / 8), dim3(kScanThreads), 0, s, tile_hist, n_tiles, P, counts);
+    e = launch_pdl_at(urgent, column_scan_kernel, dim3((P + 7) / 8), dim3(kScanThreads), 0, s, tile_hist, n_tiles,
+                      P, counts);
     if (e != cudaSuccess) return e;
     *launches += 1;
 
     const int n = T * k;
-    e = launch_pdl(assign_kernel, dim3((n + kAssignThreads - 1) / kAssignThreads), dim3(kAssignThreads),
-                   (P + 1) * sizeof(int32_t), s, phys, (const int32_t*)tile_hist, n_tiles,
-                   (const int32_t*)local_rank, (const int32_t*)counts, T, P, k, offsets, slot, src_token, src_k,
-                   err);
+    e = launch_pdl_at(urgent, assign_kernel, dim3((n + kAssignThreads - 1) / kAssignThreads),
+                      dim3(kAssignThreads), (P + 1) * sizeof(int32_t), s, phys, (const int32_t*)tile_hist, n_tiles,
+                      (const int32_t*)local_rank, (const int32_t*)counts, T, P, k, offsets, slot, src_token,
+                      src_k, err);
     if (e != cudaSuccess) return e;
     *launches += 1;
     return cudaSuccess;
