@@ -27,6 +27,7 @@
 #include <cfloat>
 #include <climits>
 
+#include "dword.cuh"
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "trace.cuh"
@@ -93,8 +94,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // Route one 32-token tile (the body shared by both plan variants).
-// Trace stages: 0 start, 1 top-k done, 2 exp done, 3 sums done, 4 gates and
-// masks done, 5 tile counts and ranks written.
+// Trace stages: 0 start, 1 top-k done, 2 gates from pairs done, 3 fp64
+// fallback done, 4 replicas and masks done, 5 tile counts and ranks written.
 template <int EPL, int WHERE>  // logits per lane = ceil(E / 32)
 __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int T, int E, int P, int k,
                                            const int32_t* __restrict__ rep_off,
@@ -103,9 +104,8 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
                                            int32_t* __restrict__ tile_hist, int n_tiles,
                                            int32_t* __restrict__ local_rank, int32_t* __restrict__ err,
                                            unsigned char* smem, int tile) {
-    double* e64 = reinterpret_cast<double*>(smem);                          // [32*k]
-    double* rsum = e64 + kTileTokens * k;                                   // [32] 1 / sum per token
-    float* sel_v = reinterpret_cast<float*>(rsum + kTileTokens);            // [32*k]
+    float2* s_exp = reinterpret_cast<float2*>(smem);                             // exp(m / 512) table
+    float* sel_v = reinterpret_cast<float*>(s_exp + 2 * dword::kExpTableHalf + 1);  // [32*k]
     int32_t* sel_e = reinterpret_cast<int32_t*>(sel_v + kTileTokens * k);  // [32*k]
     int32_t* sel_p = sel_e + kTileTokens * k;                               // [32*k]
     uint32_t* mask = reinterpret_cast<uint32_t*>(sel_p + kTileTokens * k);  // [P]
@@ -113,6 +113,7 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     int32_t* s_ids = s_off + (E + 1);                                       // [P]
 
     ROUTE_MARK(0);
+    for (int i = threadIdx.x; i <= 2 * dword::kExpTableHalf; i += kRouteThreads) s_exp[i] = dword::kExpTable[i];
     const int tl = threadIdx.x >> 5;  // this warp's token within the tile
     const int lane = threadIdx.x & 31;
     const int t0 = tile * kTileTokens;
@@ -193,26 +194,60 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     __syncthreads();
     ROUTE_MARK(1);
 
-    // ---- gates in fp64: e_j = exp(l_j - l_0) (e_0 = 1 exactly), s = sum over
-    // j ascending, gate = (float)(e_j / s) computed as e_j * (1 / s) ----
-    const int n_items = kTileTokens * k;
-    const int it = threadIdx.x;  // k <= 32: one (token, j) item per thread
-    const int itl = it / k;
-    const int ij = it - itl * k;
-    const bool item_ok = it < n_items && t0 + itl < T;
-    if (item_ok) e64[it] = (ij == 0) ? 1.0 : exp((double)sel_v[it] - (double)sel_v[itl * k]);
-    __syncthreads();
-    ROUTE_MARK(2);
-    if (threadIdx.x < kTileTokens && t0 + (int)threadIdx.x < T) {
-        double s = 0.0;
-        for (int jj = 0; jj < k; ++jj) s += e64[threadIdx.x * k + jj];
-        rsum[threadIdx.x] = 1.0 / s;
+    // ---- gates: g_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), rounded once
+    // to fp32.  Each token's k items sit in one segment of kp lanes (kp the
+    // power of two >= k, so a segment never straddles a warp).  Each lane
+    // forms d = l_j - l_0 exactly as a pair of floats and e_j = exp(d) as a
+    // pair; a butterfly over the segment sums the pairs (every lane ends with
+    // the same s: the pair sum is commutative); each lane divides e_j by s and
+    // keeps the high float if Ziv's test shows it is the correctly rounded
+    // quotient.  A token with an item the pairs cannot decide, or with
+    // l_j - l_0 < -64, is redone in fp64 as e_j = exp(d) with e_0 = 1,
+    // s = sum over j ascending and g_j = (float)(e_j / s). ----
+    const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
+    const int itl = (int)threadIdx.x / kp;  // token within the tile (>= 32: no item)
+    const int ij = (int)threadIdx.x - itl * kp;
+    const int it = itl * k + ij;
+    const bool item_ok = itl < kTileTokens && ij < k && t0 + itl < T;
+    float g = 0.0f;
+    bool slow = false;
+    {
+        dword::dw e = {0.0f, 0.0f};
+        if (item_ok) {
+            const dword::dw d = dword::two_sum(sel_v[it], -sel_v[itl * k]);
+            if (d.h == 0.0f)
+                e = {1.0f, 0.0f};  // j == 0, or a tie with the top logit
+            else if (d.h >= -64.0f)
+                e = dword::exp_dw(d.h, d.l, s_exp);
+            else
+                slow = true;  // far below the top logit (or not finite)
+        }
+        dword::dw s = e;
+        for (int off = 1; off < kp; off <<= 1) {
+            const dword::dw o = {__shfl_xor_sync(kFull, s.h, off), __shfl_xor_sync(kFull, s.l, off)};
+            s = dword::dw_add(s, o);
+        }
+        if (item_ok && !slow) {
+            const dword::dw q = dword::dw_div(e, s);
+            g = q.h;
+            slow = !dword::rounds_safely(q);
+        }
     }
-    __syncthreads();
+    ROUTE_MARK(2);
+    const unsigned slow_lanes = __ballot_sync(kFull, slow);
+    if (slow_lanes != 0u) {  // warp-uniform; rare
+        const int seg = (int)(threadIdx.x & 31) & ~(kp - 1);
+        const unsigned seg_bits = (kp == 32 ? 0xffffffffu : ((1u << kp) - 1u)) << seg;
+        const bool redo = (slow_lanes & seg_bits) != 0u && item_ok;
+        double e64 = 0.0;
+        if (redo) e64 = (ij == 0) ? 1.0 : exp((double)sel_v[it] - (double)sel_v[itl * k]);
+        double s64 = 0.0;
+        for (int jj = 0; jj < k; ++jj) s64 += __shfl_sync(kFull, e64, seg + jj);
+        if (redo) g = (float)(e64 / s64);
+    }
     ROUTE_MARK(3);
     if (item_ok) {
         const int tt = t0 + itl;
-        const float g = (float)(e64[it] * rsum[itl]);
         const int e = sel_e[it];
         int p = e;
         if (rep_off != nullptr) {
@@ -425,7 +460,33 @@ assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile
 // each), offsets, and the placement of every (t, j) copy.  Counts land in
 // shared memory (scanned in place into offsets) and, when they fit
 // (col_smem), so do the tile bases.  Data written by other CTAs is read with
-// L1-bypassing loads.
+// L1-bypassing loads.  The physical expert and in-tile rank of each thread's
+// first kTailPrefetch copies are loaded together with the columns, so the
+// tail waits for one round trip to L2 instead of two.
+constexpr int kTailPrefetch = 2;
+
+__device__ __forceinline__ void place_copy(int it, int p, int rank, int k, int P, int n, int n_tiles,
+                                           const int32_t* offs, const int32_t* colpre, int col_smem,
+                                           const int32_t* __restrict__ tile_hist, int32_t* __restrict__ slot,
+                                           int32_t* __restrict__ src_token, int32_t* __restrict__ src_k,
+                                           int32_t* __restrict__ err) {
+    const int t = it / k;
+    const int j = it - t * k;
+    int r = -1;
+    if (p >= 0 && p < P) {
+        const size_t c = (size_t)p * n_tiles + t / kTileTokens;
+        r = offs[p] + (col_smem ? colpre[c] : __ldcg(tile_hist + c)) + rank;
+    }
+    if (r < 0 || r >= n) {
+        set_error(err, MOE_DEVERR_SLOT);
+        slot[it] = -1;
+        return;
+    }
+    slot[it] = r;
+    src_token[r] = t;
+    src_k[r] = j;
+}
+
 __device__ void plan_tail(int32_t* __restrict__ tile_hist, int n_tiles, int T, int P, int k,
                           const int32_t* __restrict__ phys, const int32_t* __restrict__ local_rank,
                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
@@ -433,6 +494,14 @@ __device__ void plan_tail(int32_t* __restrict__ tile_hist, int n_tiles, int T, i
                           unsigned char* smem, int col_smem) {
     int32_t* offs = reinterpret_cast<int32_t*>(smem);  // [P+1], reuses the route scratch
     int32_t* colpre = offs + (P + 1);                   // [P, n_tiles] when col_smem
+    const int n = T * k;
+    int pre_p[kTailPrefetch], pre_rank[kTailPrefetch];
+#pragma unroll
+    for (int u = 0; u < kTailPrefetch; ++u) {
+        const int it = threadIdx.x + u * kRouteThreads;
+        pre_p[u] = (it < n) ? __ldcg(phys + it) : -1;
+        pre_rank[u] = (it < n) ? __ldcg(local_rank + it) : 0;
+    }
     for (int p = threadIdx.x; p < P; p += kRouteThreads) {
         int32_t* col = tile_hist + (size_t)p * n_tiles;
         int32_t* dst = col_smem ? colpre + (size_t)p * n_tiles : col;
@@ -453,26 +522,16 @@ __device__ void plan_tail(int32_t* __restrict__ tile_hist, int n_tiles, int T, i
     __syncthreads();
     block_scan_in_place<kRouteThreads>(offs, P);
     for (int q = threadIdx.x; q <= P; q += kRouteThreads) offsets[q] = offs[q];
-    const int n = T * k;
-    for (int it = threadIdx.x; it < n; it += kRouteThreads) {
-        const int t = it / k;
-        const int j = it - t * k;
-        const int p = __ldcg(phys + it);
-        const int rank = __ldcg(local_rank + it);
-        int r = -1;
-        if (p >= 0 && p < P) {
-            const size_t c = (size_t)p * n_tiles + t / kTileTokens;
-            r = offs[p] + (col_smem ? colpre[c] : __ldcg(tile_hist + c)) + rank;
-        }
-        if (r < 0 || r >= n) {
-            set_error(err, MOE_DEVERR_SLOT);
-            slot[it] = -1;
-            continue;
-        }
-        slot[it] = r;
-        src_token[r] = t;
-        src_k[r] = j;
+#pragma unroll
+    for (int u = 0; u < kTailPrefetch; ++u) {
+        const int it = threadIdx.x + u * kRouteThreads;
+        if (it < n)
+            place_copy(it, pre_p[u], pre_rank[u], k, P, n, n_tiles, offs, colpre, col_smem, tile_hist, slot,
+                       src_token, src_k, err);
     }
+    for (int it = threadIdx.x + kTailPrefetch * kRouteThreads; it < n; it += kRouteThreads)
+        place_copy(it, __ldcg(phys + it), __ldcg(local_rank + it), k, P, n, n_tiles, offs, colpre, col_smem,
+                   tile_hist, slot, src_token, src_k, err);
 }
 
 // Single-launch plan for batches of at most MOE_PLAN_SINGLE_MAX_TILES tiles
@@ -613,7 +672,7 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
                         int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err, int32_t* ticket,
                         cudaStream_t s, uint64_t* launches) {
     const size_t items = (size_t)kTileTokens * k;
-    size_t smem = items * (sizeof(double) + sizeof(float) + 2 * sizeof(int32_t)) + kTileTokens * sizeof(double) +
+    size_t smem = (2 * dword::kExpTableHalf + 1) * sizeof(float2) + items * (sizeof(float) + 2 * sizeof(int32_t)) +
                   (size_t)P * sizeof(uint32_t) + (size_t)(E + 1 + P) * sizeof(int32_t);
     const int epl = (E + 31) / 32;
 #define MOE_PLAN_CASE(N)                                                                                  \

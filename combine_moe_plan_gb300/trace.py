@@ -26,11 +26,11 @@ from combine_moe_plan_gb300 import moe
 
 TRACE_CTAS, TRACE_STAGES = 8192, 8
 KINDS = {
-    0: ("route_tile", ["start", "top-k", "exp", "sums", "gates+masks", "counts+ranks"]),
+    0: ("route_tile", ["start", "top-k", "gates(pairs)", "fallback", "replicas+masks", "counts+ranks"]),
     1: ("column_scan", ["start", "end"]),
     2: ("assign", ["start", "offsets", "end"]),
-    3: ("plan_single", ["start", "top-k", "exp", "sums", "gates+masks", "counts+ranks", "tail(last)",
-                        "end(last)"]),
+    3: ("plan_single", ["start", "top-k", "gates(pairs)", "fallback", "replicas+masks", "counts+ranks",
+                        "tail(last)", "end(last)"]),
     4: ("dispatch", ["start", "quantized", "slots", "stored"]),
     5: ("combine", ["start", "slots", "accumulated", "stored"]),
 }
