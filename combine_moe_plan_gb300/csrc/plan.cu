@@ -366,8 +366,14 @@ __device__ void block_offsets(const int32_t* __restrict__ counts, int P, int32_t
     }
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+    // Every warp scans the warp totals with shuffles and takes its base.
+    int tot = (lane < THREADS / 32) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, tot, off);
+        if (lane >= off) tot += o;
+    }
+    const int wbase = __shfl_sync(kFull, tot, warp) - warp_tot[warp];
     int run = wbase + incl - local;
     for (int i = 0; i < per; ++i) {
         if (lo + i < P) {
@@ -398,8 +404,14 @@ __device__ void block_scan_in_place(int32_t* a, int n) {
     }
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += warp_tot[w];
+    // Every warp scans the warp totals with shuffles and takes its base.
+    int tot = (lane < THREADS / 32) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, tot, off);
+        if (lane >= off) tot += o;
+    }
+    const int wbase = __shfl_sync(kFull, tot, warp) - warp_tot[warp];
     int run = wbase + incl - local;
     for (int i = 0; i < per; ++i) {
         if (lo + i < n) {
@@ -557,12 +569,18 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     MOE_TRACE_SM(tr_single);
     route_tile<EPL, kRouteInSingle>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
                                     n_tiles, local_rank, err, smem, blockIdx.x);
-    __threadfence();
+    // The barrier orders every thread's writes before thread 0's fence and
+    // ticket (fences are cumulative); in the last CTA, thread 0's second fence
+    // and the barrier after it order the other CTAs' results before every
+    // thread's reads of them.
     __syncthreads();
-    if (threadIdx.x == 0) last = (atomicAdd(ticket, 1) == (int)gridDim.x - 1);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = (atomicAdd(ticket, 1) == (int)gridDim.x - 1);
+        if (last) __threadfence();
+    }
     __syncthreads();
     if (!last) return;
-    __threadfence();
 
     MOE_TRACE_MARK(tr_single, 6);
     plan_tail(tile_hist, n_tiles, T, P, k, phys, local_rank, counts, offsets, slot, src_token, src_k, err, smem,
