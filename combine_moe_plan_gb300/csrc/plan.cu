@@ -40,23 +40,26 @@ MOE_TRACE_BUFFERS(tr_assign)
 namespace moe {
 namespace {
 
-// The two largest keys of a lane and their slots (lower slot first among
-// equal keys); k2 = 0 if the lane has fewer than two keys above 0.
+// The two largest keys of a lane that are not yet taken (bit r of `taken`
+// marks slot r) and their slots (lower slot first among equal keys); k2 = 0
+// if the lane has fewer than two such keys above 0.
 template <int N>
-__device__ __forceinline__ void lane_top2(const uint32_t (&key)[N], uint32_t& k1, int& r1, uint32_t& k2, int& r2) {
+__device__ __forceinline__ void lane_top2(const uint32_t (&key)[N], uint32_t taken, uint32_t& k1, int& r1,
+                                          uint32_t& k2, int& r2) {
     k1 = 0u;
     r1 = 0;
     k2 = 0u;
     r2 = 0;
 #pragma unroll
     for (int r = 0; r < N; ++r) {
-        if (key[r] > k1) {
+        const uint32_t v = ((taken >> r) & 1u) ? 0u : key[r];
+        if (v > k1) {
             k2 = k1;
             r2 = r1;
-            k1 = key[r];
+            k1 = v;
             r1 = r;
-        } else if (key[r] > k2) {
-            k2 = key[r];
+        } else if (v > k2) {
+            k2 = v;
             r2 = r;
         }
     }
@@ -93,6 +96,11 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Inverse of order_key (a -0 logit comes back as +0).
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 // Route one 32-token tile (the body shared by both plan variants).
 // Trace stages: 0 start, 1 top-k done, 2 gates from pairs done, 3 fp64
 // fallback done, 4 replicas and masks done, 5 tile counts and ranks written.
@@ -113,7 +121,15 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     int32_t* s_ids = s_off + (E + 1);                                       // [P]
 
     ROUTE_MARK(0);
-    for (int i = threadIdx.x; i <= 2 * dword::kExpTableHalf; i += kRouteThreads) s_exp[i] = dword::kExpTable[i];
+    // The exp table and the replica map go to shared memory by asynchronous
+    // copies (no registers held, no wait) while the logits are loaded; they
+    // are waited for before the barrier that ends the top-k.
+    static_assert(2 * dword::kExpTableHalf < kRouteThreads, "one exp table entry per thread");
+    if ((int)threadIdx.x <= 2 * dword::kExpTableHalf) cp_async8(s_exp + threadIdx.x, dword::kExpTable + threadIdx.x);
+    if (rep_off != nullptr) {
+        for (int i = threadIdx.x; i <= E; i += kRouteThreads) cp_async4(s_off + i, rep_off + i);
+        for (int i = threadIdx.x; i < P; i += kRouteThreads) cp_async4(s_ids + i, rep_ids + i);
+    }
     const int tl = threadIdx.x >> 5;  // this warp's token within the tile
     const int lane = threadIdx.x & 31;
     const int t0 = tile * kTileTokens;
@@ -125,24 +141,10 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     // equal floats give equal keys).  Each lane caches its two largest keys;
     // a round is one warp max-reduction of the lanes' first keys and one
     // min-reduction of the expert id among the lanes holding the maximum,
-    // after which the winning lane promotes its second key (and rescans only
-    // when it has none left).  Key 0 sits below every finite logit and marks
-    // padding and experts already taken.  The replica map is fetched into
-    // registers before the logits, so both loads are in flight together.
-    int32_t rm_off[2] = {0, 0};        // E + 1 <= 1025 entries
-    int32_t rm_ids[4] = {0, 0, 0, 0};  // P <= 4096 = 4 x kRouteThreads
-    if (rep_off != nullptr) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int i = q * kRouteThreads + threadIdx.x;
-            if (i <= E) rm_off[q] = __ldg(rep_off + i);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = q * kRouteThreads + threadIdx.x;
-            if (i < P) rm_ids[q] = __ldg(rep_ids + i);
-        }
-    }
+    // after which the winning lane marks the slot taken and promotes its
+    // second key (rescanning only when it has none left).  Key 0 sits below
+    // every finite logit and marks padding.  Lane j keeps the j-th winner and
+    // its key, whose inverse is the selected logit.
     if (t < T) {
         const float* row = logits + (size_t)t * E;
         uint32_t key[EPL];
@@ -151,46 +153,39 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
             const int e = r * 32 + lane;
             key[r] = (e < E) ? order_key(__ldg(row + e)) : 0u;
         }
-        uint32_t k1, k2;
+        uint32_t taken = 0u, k1, k2;
         int r1, r2;
-        lane_top2(key, k1, r1, k2, r2);
+        lane_top2(key, taken, k1, r1, k2, r2);
+        uint32_t cand = (uint32_t)(r1 * 32 + lane);
         int my_e = 0;
+        uint32_t my_key = 0u;
         for (int j = 0; j < k; ++j) {
             const uint32_t m = __reduce_max_sync(kFull, k1);
-            int win = (int)__reduce_min_sync(kFull, (k1 == m) ? (uint32_t)(r1 * 32 + lane) : (uint32_t)INT_MAX);
+            int win = (int)__reduce_min_sync(kFull, (k1 == m) ? cand : (uint32_t)INT_MAX);
             if (win >= E) win = 0;  // only reachable with NaN logits (outside the domain)
             if (lane == (win & 31)) {
-#pragma unroll
-                for (int r = 0; r < EPL; ++r)
-                    if (r == r1) key[r] = 0u;
+                taken |= 1u << r1;
                 if (k2 != 0u) {
                     k1 = k2;
                     r1 = r2;
                     k2 = 0u;
                 } else {
-                    lane_top2(key, k1, r1, k2, r2);
+                    lane_top2(key, taken, k1, r1, k2, r2);
                 }
+                cand = (uint32_t)(r1 * 32 + lane);
             }
-            if (lane == j) my_e = win;
+            if (lane == j) {
+                my_e = win;
+                my_key = m;
+            }
         }
         if (lane < k) {
-            sel_v[tl * k + lane] = __ldg(row + my_e);
+            sel_v[tl * k + lane] = key_value(my_key);
             sel_e[tl * k + lane] = my_e;
         }
     }
     for (int p = threadIdx.x; p < P; p += kRouteThreads) mask[p] = 0u;
-    if (rep_off != nullptr) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int i = q * kRouteThreads + threadIdx.x;
-            if (i <= E) s_off[i] = rm_off[q];
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = q * kRouteThreads + threadIdx.x;
-            if (i < P) s_ids[i] = rm_ids[q];
-        }
-    }
+    cp_async_wait_all();
     __syncthreads();
     ROUTE_MARK(1);
 
