@@ -346,6 +346,17 @@ def test_empty_batch_and_maximum_sizes():
     _custom(6, 65536, 8, 8, 2, rng.standard_normal((6, 8)))
 
 
+def test_three_launch_plan_at_maximum_shapes():
+    """More than 32 tiles (so the route / column-scan / assign kernels run)
+    at the largest shapes the API takes: E = 1024, P = 4096 (four replicas per
+    expert), k = 32 -- the route kernel's largest shared-memory footprint."""
+    rng = np.random.default_rng(11)
+    E, P = 1024, 4096
+    off = np.arange(0, P + 1, 4, dtype=np.int32)
+    ids = rng.permutation(P).astype(np.int32)
+    _custom(1100, 128, E, P, 32, rng.standard_normal((1100, E)), rep_off=off, rep_ids=ids)
+
+
 def test_bench_schedule_two_streams_full_size():
     """The bench's timed schedule at the bench workload's full size: steps
     alternate the two buffer sets on two streams, launched back to back, each
