@@ -11,8 +11,10 @@
 //   route_tile   one CTA of 32 warps per tile of 32 tokens, one warp per
 //                token: k rounds of warp arg-max by redux.sync over each
 //                lane's cached two largest keys (ties -> lower expert id).
-//                The CTA then computes the gates in fp64 with one
-//                (token, j) pair per thread, applies the replica map, and sets
+//                The CTA then computes the gates (the softmax over the k
+//                selected logits, rounded once to fp32: from float pairs, see
+//                dword.cuh, with fp64 for the rare token the pairs cannot
+//                settle), applies the replica map, and sets
 //                bit t of a shared-memory mask per physical expert.  From the
 //                mask: the tile's count per expert (popc) and each copy's rank
 //                among earlier tokens of the tile (popc of the lower bits).

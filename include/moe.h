@@ -164,7 +164,8 @@ MOE_API int moe_replica_check(const int32_t* rep_off, const int32_t* rep_ids, in
  *   rep_off  device int32 [E+1], rep_ids device int32 [P]: replica map (CSR);
  *            both NULL means physical = logical (requires P == E).
  * Per token t: the k largest logits (equal logits: lower expert id first),
- * gates = softmax over those k logits (fp64, rounded once to fp32), and the
+ * gates = softmax over those k logits, the exact value rounded once to fp32
+ * (except within about 2^-50 of an fp32 rounding midpoint), and the
  * physical replica rep_ids[rep_off[e] + t mod (rep_off[e+1] - rep_off[e])].
  * Then counts, offsets (exclusive scan, offsets[P] = T*k), slot[t,j] =
  * offsets[p] + (number of tokens before t routed to p), and the inverse
