@@ -346,6 +346,19 @@ def test_empty_batch_and_maximum_sizes():
     _custom(6, 65536, 8, 8, 2, rng.standard_normal((6, 8)))
 
 
+def test_plan_path_switch_at_32_tiles():
+    """1024 tokens (32 tiles) take the single-launch plan, 1025 (33 tiles) the
+    three launches; both on one pool, one after the other, in both orders."""
+    rng = np.random.default_rng(12)
+    E, P, k, H = 256, 288, 8, 256
+    w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
+    inp = wl.make_inputs(wl.small_variant(w, 1025))
+    pool = moe.Pool(1025, H, E, P, k, n_sets=2)
+    for T in (1024, 1025, 1024):
+        _custom(T, H, E, P, k, inp["logits"][:T], rep_off=inp["rep_off"], rep_ids=inp["rep_ids"],
+                seed=int(rng.integers(1 << 30)), T_max=1025, pool=pool)
+
+
 def test_three_launch_plan_at_maximum_shapes():
     """More than 32 tiles (so the route / column-scan / assign kernels run)
     at the largest shapes the API takes: E = 1024, P = 4096 (four replicas per
