@@ -382,45 +382,6 @@ __device__ void block_offsets(const int32_t* __restrict__ counts, int P, int32_t
     __syncthreads();
 }
 
-// In-place exclusive scan of a[0..n) in shared memory by the whole CTA;
-// a[n] receives the total.
-template <int THREADS>
-__device__ void block_scan_in_place(int32_t* a, int n) {
-    __shared__ int32_t warp_tot[THREADS / 32];
-    const int per = (n + THREADS - 1) / THREADS;
-    const int lo = threadIdx.x * per;
-    int local = 0;
-    for (int i = 0; i < per; ++i)
-        if (lo + i < n) local += a[lo + i];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(kFull, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    // Every warp scans the warp totals with shuffles and takes its base.
-    int tot = (lane < THREADS / 32) ? warp_tot[lane] : 0;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(kFull, tot, off);
-        if (lane >= off) tot += o;
-    }
-    const int wbase = __shfl_sync(kFull, tot, warp) - warp_tot[warp];
-    int run = wbase + incl - local;
-    for (int i = 0; i < per; ++i) {
-        if (lo + i < n) {
-            const int v = a[lo + i];
-            a[lo + i] = run;
-            run += v;
-        }
-    }
-    if (threadIdx.x == THREADS - 1) a[n] = wbase + incl;
-    __syncthreads();
-}
-
 constexpr int kAssignThreads = 256;
 
 __global__ void __launch_bounds__(kAssignThreads)
@@ -511,7 +472,14 @@ __device__ void plan_tail(int32_t* __restrict__ tile_hist, int n_tiles, int T, i
         pre_p[u] = (it < n) ? __ldcg(phys + it) : -1;
         pre_rank[u] = (it < n) ? __ldcg(local_rank + it) : 0;
     }
-    for (int p = threadIdx.x; p < P; p += kRouteThreads) {
+    // Each thread scans a contiguous chunk of columns and keeps the chunk's
+    // total in a register, so the scan of the counts into offsets starts at
+    // once (a warp scan, one barrier for the warp totals, one to publish).
+    const int per = (P + kRouteThreads - 1) / kRouteThreads;
+    const int p_lo = threadIdx.x * per;
+    const int p_hi = min(P, p_lo + per);
+    int chunk = 0;
+    for (int p = p_lo; p < p_hi; ++p) {
         int32_t* col = tile_hist + (size_t)p * n_tiles;
         int32_t* dst = col_smem ? colpre + (size_t)p * n_tiles : col;
         int carry = 0;
@@ -527,10 +495,40 @@ __device__ void plan_tail(int32_t* __restrict__ tile_hist, int n_tiles, int T, i
         }
         counts[p] = carry;
         offs[p] = carry;
+        chunk += carry;
+    }
+    {
+        __shared__ int32_t warp_tot[kRouteThreads / 32];
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int incl = chunk;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        static_assert(kRouteThreads == 32 * 32, "one warp total per lane");
+        int tot = warp_tot[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, tot, off);
+            if (lane >= off) tot += o;
+        }
+        const int total = __shfl_sync(kFull, tot, 31);
+        int run = __shfl_sync(kFull, tot, warp) - warp_tot[warp] + incl - chunk;
+        for (int p = p_lo; p < p_hi; ++p) {  // this thread's own entries
+            const int v = offs[p];
+            offs[p] = run;
+            offsets[p] = run;
+            run += v;
+        }
+        if (threadIdx.x == 0) {
+            offs[P] = total;
+            offsets[P] = total;
+        }
     }
     __syncthreads();
-    block_scan_in_place<kRouteThreads>(offs, P);
-    for (int q = threadIdx.x; q <= P; q += kRouteThreads) offsets[q] = offs[q];
 #pragma unroll
     for (int u = 0; u < kTailPrefetch; ++u) {
         const int it = threadIdx.x + u * kRouteThreads;
