@@ -88,7 +88,6 @@ constexpr int kRouteThreads = 32 * kTileTokens;  // one warp per token of the ti
 #define MOE_PLAN_SINGLE_MAX_TILES 32
 #endif
 
-
 // Monotone map of finite floats onto uint32 (a < b  <=>  key(a) < key(b));
 // -0 is folded onto +0 first, so equal values give equal keys.  Every finite
 // value maps above 0.
@@ -136,7 +135,6 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     const int lane = threadIdx.x & 31;
     const int t0 = tile * kTileTokens;
     const int t = t0 + tl;
-
 
     // ---- top-k of token t: k rounds of warp arg-max, ties -> lower id ----
     // Logits become order-preserving unsigned keys (-0 folded onto +0 so that
