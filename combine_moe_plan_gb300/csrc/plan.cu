@@ -102,10 +102,13 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
-// Route one 32-token tile (the body shared by both plan variants).
+// Route one 32-token tile (the body shared by both plan variants) with a CTA
+// of THREADS = 32 L threads: each token's top-k runs on a segment of L lanes
+// (L = 32: a whole warp; 16 or 8 when the experts fit in at most 8 keys a
+// lane, so that small expert counts do not occupy a whole warp per token).
 // Trace stages: 0 start, 1 top-k done, 2 gates from pairs done, 3 fp64
 // fallback done, 4 replicas and masks done, 5 tile counts and ranks written.
-template <int EPL, int WHERE>  // logits per lane = ceil(E / 32)
+template <int EPL, int WHERE, int THREADS>  // EPL = logits per lane = ceil(E / L)
 __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int T, int E, int P, int k,
                                            const int32_t* __restrict__ rep_off,
                                            const int32_t* __restrict__ rep_ids, int32_t* __restrict__ topk_e,
@@ -113,6 +116,8 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
                                            int32_t* __restrict__ tile_hist, int n_tiles,
                                            int32_t* __restrict__ local_rank, int32_t* __restrict__ err,
                                            unsigned char* smem, int tile) {
+    constexpr int L = THREADS / 32;  // lanes per token
+    static_assert(L == 8 || L == 16 || L == 32, "8, 16 or 32 lanes per token");
     float2* s_exp = reinterpret_cast<float2*>(smem);                             // exp(m / 512) table
     float* sel_v = reinterpret_cast<float*>(s_exp + 2 * dword::kExpTableHalf + 1);  // [32*k]
     int32_t* sel_e = reinterpret_cast<int32_t*>(sel_v + kTileTokens * k);  // [32*k]
@@ -125,21 +130,23 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     // The exp table and the replica map go to shared memory by asynchronous
     // copies (no registers held, no wait) while the logits are loaded; they
     // are waited for before the barrier that ends the top-k.
-    static_assert(2 * dword::kExpTableHalf < kRouteThreads, "one exp table entry per thread");
-    if ((int)threadIdx.x <= 2 * dword::kExpTableHalf) cp_async8(s_exp + threadIdx.x, dword::kExpTable + threadIdx.x);
+    for (int i = threadIdx.x; i <= 2 * dword::kExpTableHalf; i += THREADS)
+        cp_async8(s_exp + i, dword::kExpTable + i);
     if (rep_off != nullptr) {
-        for (int i = threadIdx.x; i <= E; i += kRouteThreads) cp_async4(s_off + i, rep_off + i);
-        for (int i = threadIdx.x; i < P; i += kRouteThreads) cp_async4(s_ids + i, rep_ids + i);
+        for (int i = threadIdx.x; i <= E; i += THREADS) cp_async4(s_off + i, rep_off + i);
+        for (int i = threadIdx.x; i < P; i += THREADS) cp_async4(s_ids + i, rep_ids + i);
     }
-    const int tl = threadIdx.x >> 5;  // this warp's token within the tile
-    const int lane = threadIdx.x & 31;
+    const int tl = threadIdx.x / L;  // this segment's token within the tile
+    const int sl = threadIdx.x % L;  // lane within the segment
+    const unsigned seg_mask = (L == 32) ? kFull : ((1u << L) - 1u) << ((threadIdx.x & 31) & ~(L - 1));
     const int t0 = tile * kTileTokens;
     const int t = t0 + tl;
 
-    // ---- top-k of token t: k rounds of warp arg-max, ties -> lower id ----
+    // ---- top-k of token t: k rounds of segment arg-max, ties -> lower id ----
     // Logits become order-preserving unsigned keys (-0 folded onto +0 so that
-    // equal floats give equal keys).  Each lane caches its two largest keys;
-    // a round is one warp max-reduction of the lanes' first keys and one
+    // equal floats give equal keys); lane s of the segment holds experts
+    // s, s + L, s + 2L, ...  Each lane caches its two largest keys; a round
+    // is one max-reduction of the lanes' first keys over the segment and one
     // min-reduction of the expert id among the lanes holding the maximum,
     // after which the winning lane marks the slot taken and promotes its
     // second key (rescanning only when it has none left).  Key 0 sits below
@@ -150,20 +157,20 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
         uint32_t key[EPL];
 #pragma unroll
         for (int r = 0; r < EPL; ++r) {
-            const int e = r * 32 + lane;
+            const int e = r * L + sl;
             key[r] = (e < E) ? order_key(__ldg(row + e)) : 0u;
         }
         uint32_t taken = 0u, k1, k2;
         int r1, r2;
         lane_top2(key, taken, k1, r1, k2, r2);
-        uint32_t cand = (uint32_t)(r1 * 32 + lane);
+        uint32_t cand = (uint32_t)(r1 * L + sl);
         int my_e = 0;
         uint32_t my_key = 0u;
         for (int j = 0; j < k; ++j) {
-            const uint32_t m = __reduce_max_sync(kFull, k1);
-            int win = (int)__reduce_min_sync(kFull, (k1 == m) ? cand : (uint32_t)INT_MAX);
+            const uint32_t m = __reduce_max_sync(seg_mask, k1);
+            int win = (int)__reduce_min_sync(seg_mask, (k1 == m) ? cand : (uint32_t)INT_MAX);
             if (win >= E) win = 0;  // only reachable with NaN logits (outside the domain)
-            if (lane == (win & 31)) {
+            if (sl == (win & (L - 1))) {
                 taken |= 1u << r1;
                 if (k2 != 0u) {
                     k1 = k2;
@@ -172,19 +179,19 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
                 } else {
                     lane_top2(key, taken, k1, r1, k2, r2);
                 }
-                cand = (uint32_t)(r1 * 32 + lane);
+                cand = (uint32_t)(r1 * L + sl);
             }
-            if (lane == j) {
+            if (sl == j) {
                 my_e = win;
                 my_key = m;
             }
         }
-        if (lane < k) {
-            sel_v[tl * k + lane] = key_value(my_key);
-            sel_e[tl * k + lane] = my_e;
+        if (sl < k) {
+            sel_v[tl * k + sl] = key_value(my_key);
+            sel_e[tl * k + sl] = my_e;
         }
     }
-    for (int p = threadIdx.x; p < P; p += kRouteThreads) mask[p] = 0u;
+    for (int p = threadIdx.x; p < P; p += THREADS) mask[p] = 0u;
     cp_async_wait_all();
     __syncthreads();
     ROUTE_MARK(1);
@@ -199,7 +206,7 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     // quotient.  A token with an item the pairs cannot decide, or with
     // l_j - l_0 < -64, is redone in fp64 as e_j = exp(d) with e_0 = 1,
     // s = sum over j ascending and g_j = (float)(e_j / s). ----
-    const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
+    const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));  // 32 kp <= THREADS (host's choice of L)
     const int itl = (int)threadIdx.x / kp;  // token within the tile (>= 32: no item)
     const int ij = (int)threadIdx.x - itl * kp;
     const int it = itl * k + ij;
@@ -271,7 +278,7 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     ROUTE_MARK(4);
 
     // ---- tile histogram (expert-major) and in-tile ranks ----
-    for (int p = threadIdx.x; p < P; p += kRouteThreads)
+    for (int p = threadIdx.x; p < P; p += THREADS)
         tile_hist[(size_t)p * n_tiles + tile] = __popc(mask[p]);
     if (item_ok) {
         const int p = sel_p[it];
@@ -280,13 +287,15 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     ROUTE_MARK(5);
 }
 
-// Two CTAs per SM caps the kernel at 32 registers a thread (a few spills at
-// EPL >= 8).  Uncapped, one 1024-thread CTA took the whole register file of
-// its SM, so while it ran no dispatch or combine CTA of the other buffer set
-// could share that SM; with half the file left free the pipelined step is
-// about 2.5 us shorter at 4096 tokens and the plan alone no slower.
-template <int EPL>
-__global__ void __launch_bounds__(kRouteThreads, 2)
+// 2048 / THREADS CTAs per SM caps the kernel at 32 registers a thread (a few
+// spills at 8 or more keys a lane).  Uncapped, one 1024-thread CTA took the
+// whole register file of its SM, so while it ran no dispatch or combine CTA of
+// the other buffer set could share that SM; with half the file left free the
+// pipelined step is about 2.5 us shorter at 4096 tokens and the plan alone no
+// slower.  Smaller CTAs (8 or 16 lanes a token, for small expert counts) take
+// a quarter or half of that register file.
+template <int EPL, int THREADS>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS)
 route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
                   const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
                   int32_t* __restrict__ topk_e, float* __restrict__ gates,
@@ -296,8 +305,8 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     grid_dependency_sync();
     allow_dependents();
     MOE_TRACE_SM(tr_route);
-    route_tile<EPL, kRouteInRoute>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
-                                   n_tiles, local_rank, err, smem, blockIdx.x);
+    route_tile<EPL, kRouteInRoute, THREADS>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
+                                            tile_hist, n_tiles, local_rank, err, smem, blockIdx.x);
 }
 
 // One warp: exclusive scan of tile_hist[p, :] in place, counts[p] = column
@@ -560,8 +569,8 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     grid_dependency_sync();
     allow_dependents();
     MOE_TRACE_SM(tr_single);
-    route_tile<EPL, kRouteInSingle>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
-                                    n_tiles, local_rank, err, smem, blockIdx.x);
+    route_tile<EPL, kRouteInSingle, kRouteThreads>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
+                                                   tile_hist, n_tiles, local_rank, err, smem, blockIdx.x);
     // The barrier orders every thread's writes before thread 0's fence and
     // ticket (fences are cumulative); in the last CTA, thread 0's second fence
     // and the barrier after it order the other CTAs' results before every
@@ -594,48 +603,43 @@ cudaError_t smem_attr(K kernel, size_t smem) {
 }
 
 template <int EPL>
-cudaError_t launch_plan_epl(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
-                            const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys,
-                            int32_t* tile_hist, int32_t* local_rank, int32_t* counts, int32_t* offsets,
-                            int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err, int32_t* ticket,
-                            size_t smem, cudaStream_t s, uint64_t* launches) {
-    const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
-    // The plan is latency-bound and on its stream's critical path; bandwidth-
-    // bound kernels of other streams (the other buffer set's dispatch and
-    // combine) keep HBM busy meanwhile.  At the most urgent priority the block
-    // scheduler places the plan's CTAs ahead of their queued CTAs, so the plan
-    // is not stretched by waiting for SM slots.
-    const int urgent = most_urgent_priority();
+cudaError_t launch_single(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
+                          const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys, int32_t* tile_hist,
+                          int32_t* local_rank, int32_t* counts, int32_t* offsets, int32_t* slot,
+                          int32_t* src_token, int32_t* src_k, int32_t* err, int32_t* ticket, size_t smem,
+                          int n_tiles, int urgent, cudaStream_t s) {
+    int col_smem = 0;
+    const size_t smem1 = tail_smem(smem, P, n_tiles, &col_smem);
     cudaError_t e;
-    if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
-        int col_smem = 0;
-        const size_t smem1 = tail_smem(smem, P, n_tiles, &col_smem);
-        if ((e = smem_attr(plan_single_kernel<EPL>, smem1)) != cudaSuccess) return e;
-        e = launch_pdl_at(urgent, plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem1, s, logits,
-                          T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank,
-                          counts, offsets, slot, src_token, src_k, err, ticket, col_smem);
-        if (e == cudaSuccess) *launches += 1;
-        return e;
+    if ((e = smem_attr(plan_single_kernel<EPL>, smem1)) != cudaSuccess) return e;
+    return launch_pdl_at(urgent, plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem1, s, logits, T,
+                         E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, counts,
+                         offsets, slot, src_token, src_k, err, ticket, col_smem);
+}
+
+template <int EPL, int THREADS>
+cudaError_t launch_route(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
+                         const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys, int32_t* tile_hist,
+                         int32_t* local_rank, int32_t* err, size_t smem, int n_tiles, int urgent, cudaStream_t s) {
+    cudaError_t e;
+    if ((e = smem_attr(route_tile_kernel<EPL, THREADS>, smem)) != cudaSuccess) return e;
+    return launch_pdl_at(urgent, route_tile_kernel<EPL, THREADS>, dim3(n_tiles), dim3(THREADS), smem, s, logits,
+                         T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, err);
+}
+
+// The route kernel for `epl` keys a lane (a power of two up to 32 / 8).
+template <int THREADS, typename... A>
+cudaError_t launch_route_epl(int epl, A... a) {
+    if (epl <= 1) return launch_route<1, THREADS>(a...);
+    if (epl <= 2) return launch_route<2, THREADS>(a...);
+    if (epl <= 4) return launch_route<4, THREADS>(a...);
+    if constexpr (THREADS == kRouteThreads) {
+        if (epl <= 8) return launch_route<8, THREADS>(a...);
+        if (epl <= 16) return launch_route<16, THREADS>(a...);
+        return launch_route<32, THREADS>(a...);
+    } else {
+        return launch_route<8, THREADS>(a...);
     }
-    if ((e = smem_attr(route_tile_kernel<EPL>, smem)) != cudaSuccess) return e;
-    e = launch_pdl_at(urgent, route_tile_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem, s, logits, T, E,
-                      P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, err);
-    if (e != cudaSuccess) return e;
-    *launches += 1;
-
-    e = launch_pdl_at(urgent, column_scan_kernel, dim3((P + 7) / 8), dim3(kScanThreads), 0, s, tile_hist, n_tiles,
-                      P, counts);
-    if (e != cudaSuccess) return e;
-    *launches += 1;
-
-    const int n = T * k;
-    e = launch_pdl_at(urgent, assign_kernel, dim3((n + kAssignThreads - 1) / kAssignThreads),
-                      dim3(kAssignThreads), (P + 1) * sizeof(int32_t), s, phys, (const int32_t*)tile_hist, n_tiles,
-                      (const int32_t*)local_rank, (const int32_t*)counts, T, P, k, offsets, slot, src_token,
-                      src_k, err);
-    if (e != cudaSuccess) return e;
-    *launches += 1;
-    return cudaSuccess;
 }
 
 // Shared memory for the single-launch tail: offsets and, when they fit, the
@@ -683,20 +687,63 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
                         int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err, int32_t* ticket,
                         cudaStream_t s, uint64_t* launches) {
     const size_t items = (size_t)kTileTokens * k;
-    size_t smem = (2 * dword::kExpTableHalf + 1) * sizeof(float2) + items * (sizeof(float) + 2 * sizeof(int32_t)) +
-                  (size_t)P * sizeof(uint32_t) + (size_t)(E + 1 + P) * sizeof(int32_t);
-    const int epl = (E + 31) / 32;
-#define MOE_PLAN_CASE(N)                                                                                  \
-    return launch_plan_epl<N>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,      \
-                              local_rank, counts, offsets, slot, src_token, src_k, err, ticket, smem, s, \
-                              launches)
-    if (epl <= 1) MOE_PLAN_CASE(1);
-    if (epl <= 2) MOE_PLAN_CASE(2);
-    if (epl <= 4) MOE_PLAN_CASE(4);
-    if (epl <= 8) MOE_PLAN_CASE(8);
-    if (epl <= 16) MOE_PLAN_CASE(16);
-    MOE_PLAN_CASE(32);
-#undef MOE_PLAN_CASE
+    const size_t smem = (2 * dword::kExpTableHalf + 1) * sizeof(float2) +
+                        items * (sizeof(float) + 2 * sizeof(int32_t)) + (size_t)P * sizeof(uint32_t) +
+                        (size_t)(E + 1 + P) * sizeof(int32_t);
+    const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
+    // The plan is latency-bound and on its stream's critical path; bandwidth-
+    // bound kernels of other streams (the other buffer set's dispatch and
+    // combine) keep HBM busy meanwhile.  At the most urgent priority the block
+    // scheduler places the plan's CTAs ahead of their queued CTAs, so the plan
+    // is not stretched by waiting for SM slots.
+    const int urgent = most_urgent_priority();
+    cudaError_t e;
+    if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
+        const int epl = (E + 31) / 32;
+#define MOE_SINGLE_CASE(N)                                                                                      \
+    e = launch_single<N>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, local_rank, counts, \
+                         offsets, slot, src_token, src_k, err, ticket, smem, n_tiles, urgent, s)
+        if (epl <= 1) MOE_SINGLE_CASE(1);
+        else if (epl <= 2) MOE_SINGLE_CASE(2);
+        else if (epl <= 4) MOE_SINGLE_CASE(4);
+        else if (epl <= 8) MOE_SINGLE_CASE(8);
+        else if (epl <= 16) MOE_SINGLE_CASE(16);
+        else MOE_SINGLE_CASE(32);
+#undef MOE_SINGLE_CASE
+        if (e == cudaSuccess) *launches += 1;
+        return e;
+    }
+
+    // Lanes per token in the route kernel: the fewest of 8, 16, 32 that keep
+    // at most 8 keys a lane and leave a lane per (token, j) for the gates.
+    const int kp = k <= 1 ? 1 : 1 << (32 - __builtin_clz((unsigned)(k - 1)));
+    const int L = (E <= 64 && kp <= 8) ? 8 : (E <= 128 && kp <= 16) ? 16 : 32;
+    const int epl = (E + L - 1) / L;
+    if (L == 8)
+        e = launch_route_epl<256>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
+                                  local_rank, err, smem, n_tiles, urgent, s);
+    else if (L == 16)
+        e = launch_route_epl<512>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
+                                  local_rank, err, smem, n_tiles, urgent, s);
+    else
+        e = launch_route_epl<kRouteThreads>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
+                                            tile_hist, local_rank, err, smem, n_tiles, urgent, s);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+
+    e = launch_pdl_at(urgent, column_scan_kernel, dim3((P + 7) / 8), dim3(kScanThreads), 0, s, tile_hist, n_tiles,
+                      P, counts);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+
+    const int n = T * k;
+    e = launch_pdl_at(urgent, assign_kernel, dim3((n + kAssignThreads - 1) / kAssignThreads),
+                      dim3(kAssignThreads), (P + 1) * sizeof(int32_t), s, phys, (const int32_t*)tile_hist, n_tiles,
+                      (const int32_t*)local_rank, (const int32_t*)counts, T, P, k, offsets, slot, src_token,
+                      src_k, err);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+    return cudaSuccess;
 }
 
 }  // namespace moe
