@@ -10,8 +10,10 @@
 // does not depend on scheduling.
 //
 // GPU mapping: one warp per (token, 256-element segment); a lane owns one
-// 8-element chunk (16 bytes) of every copy and keeps up to 8 copies' 16-byte
-// loads in flight before it accumulates them in order.
+// 8-element chunk (16 bytes) of every copy and keeps KB = min(k, 8) copies'
+// 16-byte loads in flight before it accumulates them in order.  KB is a
+// template parameter, so a smaller k holds fewer registers and more CTAs fit
+// on an SM (k = 6: five CTAs instead of four, 3.5 % faster at hidden 2048).
 #include "moe_internal.h"
 #include "ptx.cuh"
 #include "trace.cuh"
@@ -24,8 +26,8 @@ namespace {
 constexpr int kCombineThreads = 256;  // 8 warps
 constexpr int kChunks = 1;            // 16-byte chunks per lane per item
 constexpr int kSegElems = 32 * 8 * kChunks;
-constexpr int kBatch = 8;             // copies loaded before accumulating
 
+template <int KB>  // copies loaded before accumulating
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ slot,
                const float* __restrict__ gates, int T, int H, int k, uint16_t* __restrict__ y,
@@ -72,10 +74,10 @@ combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ 
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[c][e] = 0.0f;
 
-    for (int jb = 0; jb < k; jb += kBatch) {
-        uint4 d[kBatch][kChunks];
+    for (int jb = 0; jb < k; jb += KB) {
+        uint4 d[KB][kChunks];
 #pragma unroll
-        for (int jj = 0; jj < kBatch; ++jj) {
+        for (int jj = 0; jj < KB; ++jj) {
             const int j = jb + jj;
             const int r = __shfl_sync(kFull, my_slot, j & 31);
 #pragma unroll
@@ -85,7 +87,7 @@ combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ 
             }
         }
 #pragma unroll
-        for (int jj = 0; jj < kBatch; ++jj) {
+        for (int jj = 0; jj < KB; ++jj) {
             const int j = jb + jj;
             const float g = __shfl_sync(kFull, my_gate, j & 31);
             if (j < k) {
@@ -129,8 +131,21 @@ cudaError_t launch_combine(const uint16_t* ex_out, const int32_t* slot, const fl
                            uint16_t* y, int32_t* err, cudaStream_t s, uint64_t* launches) {
     const long long items = (long long)T * ((H + kSegElems - 1) / kSegElems);
     const long long blocks = (items + (kCombineThreads / 32) - 1) / (kCombineThreads / 32);
-    cudaError_t e = launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineThreads), 0, s, ex_out, slot,
-                               gates, T, H, k, y, err);
+    cudaError_t e;
+#define MOE_COMBINE_CASE(KB)                                                                                    \
+    e = launch_pdl(combine_kernel<KB>, dim3((unsigned)blocks), dim3(kCombineThreads), 0, s, ex_out, slot, gates, \
+                   T, H, k, y, err)
+    switch (k < 8 ? k : 8) {
+        case 1: MOE_COMBINE_CASE(1); break;
+        case 2: MOE_COMBINE_CASE(2); break;
+        case 3: MOE_COMBINE_CASE(3); break;
+        case 4: MOE_COMBINE_CASE(4); break;
+        case 5: MOE_COMBINE_CASE(5); break;
+        case 6: MOE_COMBINE_CASE(6); break;
+        case 7: MOE_COMBINE_CASE(7); break;
+        default: MOE_COMBINE_CASE(8); break;
+    }
+#undef MOE_COMBINE_CASE
     if (e == cudaSuccess) *launches += 1;
     return e;
 }
