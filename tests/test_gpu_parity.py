@@ -346,6 +346,16 @@ def test_empty_batch_and_maximum_sizes():
     _custom(6, 65536, 8, 8, 2, rng.standard_normal((6, 8)))
 
 
+@pytest.mark.parametrize("k", list(range(1, 13)))
+def test_combine_every_batch_width(k):
+    """Combine keeps min(k, 8) copies in flight (one kernel per width); every
+    k from 1 to 12, so each width and k > 8 (a partial second batch) run, at
+    H = 384 (the second 256-element segment is half full)."""
+    rng = np.random.default_rng(300 + k)
+    E = max(16, k)
+    _custom(45, 384, E, E, k, rng.standard_normal((45, E)), seed=k)
+
+
 def test_plan_path_switch_at_32_tiles():
     """1024 tokens (32 tiles) take the single-launch plan, 1025 (33 tiles) the
     three launches; both on one pool, one after the other, in both orders."""
