@@ -356,6 +356,19 @@ def test_combine_every_batch_width(k):
     _custom(45, 384, E, E, k, rng.standard_normal((45, E)), seed=k)
 
 
+@pytest.mark.parametrize("E", [8, 16, 32, 64, 100, 128, 200, 512])
+@pytest.mark.parametrize("k", [2, 6, 12])
+def test_route_lane_segments(E, k):
+    """The three-launch route kernel gives each token 8, 16 or 32 lanes
+    (the fewest that keep at most 8 logits a lane and a lane per gate);
+    1100 tokens (35 tiles) over expert counts and k that select every
+    (lanes, logits-per-lane) variant, checked in full against the oracle."""
+    if k > E:
+        pytest.skip("k > E")
+    rng = np.random.default_rng(1000 * k + E)
+    _custom(1100, 128, E, E, k, rng.standard_normal((1100, E)), seed=E + k)
+
+
 def test_plan_path_switch_at_32_tiles():
     """1024 tokens (32 tiles) take the single-launch plan, 1025 (33 tiles) the
     three launches; both on one pool, one after the other, in both orders."""
