@@ -155,3 +155,49 @@ def test_binding_has_no_oracle_or_cpu_path():
     pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle)|moe_oracle|libmoe_oracle", re.M)
     for f in list(pkg.glob("*.py")) + list(pkg.glob("csrc/*")):
         assert not pat.search(f.read_text()), f
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe.h"
+
+int main(void) {
+    moe_desc d;
+    size_t bytes = 0;
+    int32_t off[3] = {0, 2, 3}, ids[3] = {2, 0, 1}, bad_ids[3] = {0, 0, 1};
+    d.T_max = 4096; d.H = 7168; d.E = 256; d.P = 288; d.k = 8; d.group = 128; d.n_sets = 2;
+    if (moe_pool_bytes(&d, &bytes) != MOE_OK || bytes == 0) return 1;
+    if (strcmp(moe_status_str(MOE_OK), "ok") != 0) return 2;
+    if (moe_replica_check(off, ids, 2, 3) != MOE_OK) return 3;
+    if (moe_replica_check(off, bad_ids, 2, 3) != MOE_ERR_REPLICA) return 4;
+    d.k = 0;
+    if (moe_pool_bytes(&d, &bytes) != MOE_ERR_SIZE) return 5;
+    printf("%zu\n", bytes);
+    return 0;
+}
+"""
+
+
+def test_header_is_c_and_links_from_c(L, tmp_path):
+    """include/moe.h compiles as ISO C11 with every warning an error, and a C
+    program links against libmoe.so and calls its host-only entry points:
+    the same pool size as the binding reports, status strings, replica-map
+    checks, argument rejection."""
+    import os
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(moe.LIB_PATH)
+    inc = os.path.dirname(moe.HEADER)
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{inc}", str(src), "-o", str(exe),
+                    f"-L{libdir}", "-l:libmoe.so", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    rc, n = _bytes(L, _desc(T=4096, H=7168, E=256, P=288, k=8))
+    assert rc == 0 and int(out.stdout.strip()) == n
