@@ -369,6 +369,37 @@ def test_route_lane_segments(E, k):
     _custom(1100, 128, E, E, k, rng.standard_normal((1100, E)), seed=E + k)
 
 
+@pytest.mark.parametrize("T", [64, 1100])
+def test_non_finite_logits_keep_a_valid_placement(T):
+    """NaN and +-Inf logits are outside the method's domain (the oracle
+    rejects them; gates and y are unspecified), but both plan paths must
+    still pick k distinct experts per token in range, place every copy
+    exactly once, set no device error bit, and leave the pool usable: a
+    finite batch right after matches the oracle."""
+    rng = np.random.default_rng(77)
+    E, k, H = 64, 6, 256
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    flat = logits.reshape(-1)
+    pos = rng.choice(flat.size, size=flat.size // 20, replace=False)
+    flat[pos[0::3]] = np.nan
+    flat[pos[1::3]] = np.inf
+    flat[pos[2::3]] = -np.inf
+    pool = moe.Pool(T, H, E, E, k, n_sets=1)
+    x = dev_bf16(wl.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)))
+    pool.plan(dev(logits))
+    pool.dispatch(x)
+    pool.combine(T)
+    assert pool.check() == 0
+    v = pool.view(0)
+    topk = v["topk_e"][:T].cpu().numpy()
+    assert topk.min() >= 0 and topk.max() < E
+    assert all(len(set(r)) == k for r in topk.tolist())
+    slots = v["slot"][:T].cpu().numpy()
+    assert sorted(slots.ravel().tolist()) == list(range(T * k))
+    finite = rng.standard_normal((T, E)).astype(np.float32)
+    _custom(T, H, E, E, k, finite, pool=pool, T_max=T)
+
+
 def test_plan_path_switch_at_32_tiles():
     """1024 tokens (32 tiles) take the single-launch plan, 1025 (33 tiles) the
     three launches; both on one pool, one after the other, in both orders."""
