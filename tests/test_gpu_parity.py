@@ -371,11 +371,11 @@ def test_route_lane_segments(E, k):
 
 @pytest.mark.parametrize("T", [64, 1100])
 def test_non_finite_logits_keep_a_valid_placement(T):
-    """NaN and +-Inf logits are outside the method's domain (the oracle
-    rejects them; gates and y are unspecified), but both plan paths must
-    still pick k distinct experts per token in range, place every copy
-    exactly once, set no device error bit, and leave the pool usable: a
-    finite batch right after matches the oracle."""
+    """NaN and +-Inf logits and activations are outside the method's domain
+    (the oracle rejects them; gates, codes and y are unspecified), but both
+    plan paths must still pick k distinct experts per token in range, place
+    every copy exactly once, set no device error bit, and leave the pool
+    usable: a finite batch right after matches the oracle."""
     rng = np.random.default_rng(77)
     E, k, H = 64, 6, 256
     logits = rng.standard_normal((T, E)).astype(np.float32)
@@ -385,7 +385,10 @@ def test_non_finite_logits_keep_a_valid_placement(T):
     flat[pos[1::3]] = np.inf
     flat[pos[2::3]] = -np.inf
     pool = moe.Pool(T, H, E, E, k, n_sets=1)
-    x = dev_bf16(wl.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)))
+    xf = rng.standard_normal((T, H)).astype(np.float32)
+    xf[rng.random((T, H)) < 0.01] = np.nan  # non-finite activations too: codes and scales unspecified
+    xf[rng.random((T, H)) < 0.01] = np.inf
+    x = dev_bf16(wl.f32_to_bf16_bits(xf))
     pool.plan(dev(logits))
     pool.dispatch(x)
     pool.combine(T)
