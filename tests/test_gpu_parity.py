@@ -403,6 +403,38 @@ def test_non_finite_logits_keep_a_valid_placement(T):
     _custom(T, H, E, E, k, finite, pool=pool, T_max=T)
 
 
+def test_step_host_matches_oracle():
+    """moe_step_host: logits and x from pinned host memory, plan, dispatch,
+    expert outputs from the host (or the identity stand-in), combine, y back
+    to the host.  Four steps alternate the two sets on two streams with their
+    own inputs; every y and plan is checked against the oracle."""
+    w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 300)
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    steps = []
+    for i in range(4):
+        inp = wl.make_inputs(w, seed=40 + i)
+        h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+        h_x = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+        h_ex = torch.from_numpy(inp["ex_out"][: w.T * w.k].view(np.int16)).pin_memory() if i % 2 else None
+        h_y = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
+        ro, ri = dev(inp["rep_off"]), dev(inp["rep_ids"])
+        steps.append((inp, h_logits, h_x, h_ex, h_y, ro, ri))
+    for i, (inp, h_logits, h_x, h_ex, h_y, ro, ri) in enumerate(steps[:2]):
+        pool.step_host(h_logits, h_x, h_y, h_ex, ro, ri, buf=i, stream=streams[i])
+    torch.cuda.synchronize()
+    for i, (inp, h_logits, h_x, h_ex, h_y, ro, ri) in enumerate(steps):
+        if i >= 2:
+            pool.step_host(h_logits, h_x, h_y, h_ex, ro, ri, buf=i % 2, stream=streams[i % 2])
+            torch.cuda.synchronize()
+        ex = None if h_ex is None else inp["ex_out"][: w.T * w.k]
+        ref = oracle.forward(inp["logits"], inp["x"], w.k, inp["rep_off"], inp["rep_ids"], w.P, ex_out=ex)
+        assert_y_close(h_y.numpy().view(np.uint16), ref["y"], f"step {i}")
+        v = pool.view(i % 2)
+        np.testing.assert_array_equal(v["slot"][: w.T].cpu().numpy(), ref["slot"])
+    assert pool.check() == 0
+
+
 def test_plan_path_switch_at_32_tiles():
     """1024 tokens (32 tiles) take the single-launch plan, 1025 (33 tiles) the
     three launches; both on one pool, one after the other, in both orders."""
