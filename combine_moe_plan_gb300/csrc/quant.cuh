@@ -1,7 +1,5 @@
 // quant.cuh -- the dispatch data step for one warp and one 512-element
 // segment of a token row: load, per-128 INT8 quantization, scatter.
-// Shared by the dispatch kernel and the fused small-batch plan + dispatch
-// kernel, so both write identical codes.
 //
 // CloudMatrix384 write-up, "FusedDispatch and FusedCombine": early INT8
 // quantization (per token; here one fp32 scale per 128 elements) and direct
