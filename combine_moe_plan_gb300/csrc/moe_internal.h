@@ -59,10 +59,48 @@ cudaError_t launch_pdl_at(int priority, void (*kernel)(KArgs...), dim3 grid, dim
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// As launch_pdl_at, with the grid launched as thread-block clusters of
+// `cluster_x` CTAs (cudaLaunchAttributeClusterDimension).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(int priority, unsigned cluster_x, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                               size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[3];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    attr[2].id = cudaLaunchAttributePriority;
+    attr[2].val.priority = priority;
+    cfg.attrs = attr;
+    cfg.numAttrs = priority != 0 ? 3 : 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                        Args... args) {
     return launch_pdl_at(0, kernel, grid, block, smem, s, args...);
+}
+
+// Whether the current device launches thread-block clusters (looked up once).
+inline bool cluster_launch_supported() {
+    static const bool v = [] {
+        int dev = 0, ok = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&ok, cudaDevAttrClusterLaunch, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        return ok != 0;
+    }();
+    return v;
 }
 
 // The most urgent launch priority the device offers (cudaDeviceGetStreamPriorityRange's

@@ -67,8 +67,9 @@ __device__ __forceinline__ void lane_top2(const uint32_t (&key)[N], uint32_t tak
     }
 }
 
-// Which kernel a route_tile call belongs to (its trace slice).
-constexpr int kRouteInRoute = 0, kRouteInSingle = 1;
+// Which kernel a route_tile call belongs to (its trace slice; the cluster
+// plan keeps tile counts and ranks in shared memory instead of writing them).
+constexpr int kRouteInRoute = 0, kRouteInSingle = 1, kRouteInCluster = 2;
 
 #ifdef MOE_TRACE
 // Stage stamps of route_tile go to the slice of the kernel that called it.
@@ -278,11 +279,13 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     ROUTE_MARK(4);
 
     // ---- tile histogram (expert-major) and in-tile ranks ----
-    for (int p = threadIdx.x; p < P; p += THREADS)
-        tile_hist[(size_t)p * n_tiles + tile] = __popc(mask[p]);
-    if (item_ok) {
-        const int p = sel_p[it];
-        local_rank[(size_t)(t0 + itl) * k + ij] = (p >= 0) ? __popc(mask[p] & ((1u << itl) - 1u)) : 0;
+    if (WHERE != kRouteInCluster) {
+        for (int p = threadIdx.x; p < P; p += THREADS)
+            tile_hist[(size_t)p * n_tiles + tile] = __popc(mask[p]);
+        if (item_ok) {
+            const int p = sel_p[it];
+            local_rank[(size_t)(t0 + itl) * k + ij] = (p >= 0) ? __popc(mask[p] & ((1u << itl) - 1u)) : 0;
+        }
     }
     ROUTE_MARK(5);
 }
@@ -591,6 +594,123 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     MOE_TRACE_MARK(tr_single, 7);
 }
 
+// Batches of at most kClusterTiles tiles (the decode regime), launched as one
+// thread-block cluster of one CTA per tile.  Every CTA routes its tile (the
+// route_tile body) and keeps its per-expert token masks in shared memory;
+// after the cluster barrier each CTA reads every tile's masks over
+// distributed shared memory, so it knows, per physical expert, the copies in
+// earlier tiles (its tile base) and in all tiles (the counts, scanned into the
+// offsets), and places its own tile's copies.  No ticket, no single-CTA tail,
+// no global tile counts or ranks.  Trace stages 0-5 as route_tile; 6 cluster
+// barrier passed, 7 copies placed.
+constexpr int kClusterTiles = 8;  // the portable cluster size
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteThreads)
+plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
+                    const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
+                    int32_t* __restrict__ topk_e, float* __restrict__ gates, int32_t* __restrict__ phys,
+                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
+                    int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int32_t warp_tot[kRouteThreads / 32];
+    grid_dependency_sync();
+    allow_dependents();
+    MOE_TRACE_SM(tr_single);
+    const int tile = (int)cluster_ctarank();  // the grid is one cluster
+    route_tile<EPL, kRouteInCluster, kRouteThreads>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
+                                                    nullptr, (int)gridDim.x, nullptr, err, smem, tile);
+    // route_tile's shared-memory layout: exp table, sel_v, sel_e, sel_p [32k],
+    // masks [P], replica offsets [E+1] and ids [P]; then this kernel's arrays.
+    const int32_t* sel_p = reinterpret_cast<const int32_t*>(
+                               reinterpret_cast<float2*>(smem) + 2 * dword::kExpTableHalf + 1) +
+                           2 * kTileTokens * k;
+    const uint32_t* mask = reinterpret_cast<const uint32_t*>(sel_p + kTileTokens * k);
+    int32_t* s_base = const_cast<int32_t*>(reinterpret_cast<const int32_t*>(mask + P)) + (E + 1) + P;  // [P]
+    int32_t* offs = s_base + P;                                                                         // [P+1]
+
+    cluster_sync();  // every tile's masks are complete and visible in the cluster
+    MOE_TRACE_MARK(tr_single, 6);
+
+    // Per physical expert: copies in earlier tiles and in all tiles.  Each
+    // thread takes a contiguous chunk of experts and keeps its chunk's total
+    // in a register for the scan into offsets.
+    const int n_cta = (int)gridDim.x;
+    const int per = (P + kRouteThreads - 1) / kRouteThreads;
+    const int p_lo = threadIdx.x * per;
+    const int p_hi = min(P, p_lo + per);
+    int chunk = 0;
+    for (int p = p_lo; p < p_hi; ++p) {
+        int total = 0, before = 0;
+        for (int c = 0; c < n_cta; ++c) {
+            const int cnt = __popc(ld_cluster_shared_u32(mask + p, (uint32_t)c));
+            before += (c < tile) ? cnt : 0;
+            total += cnt;
+        }
+        s_base[p] = before;
+        offs[p] = total;
+        if (tile == 0) counts[p] = total;
+        chunk += total;
+    }
+    cluster_arrive();  // done reading the other CTAs' masks (waited for before exit)
+
+    // Exclusive scan of the totals into offs (warp scan, one barrier for the
+    // warp totals, one to publish).
+    {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        int incl = chunk;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        static_assert(kRouteThreads == 32 * 32, "one warp total per lane");
+        int tot = warp_tot[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(kFull, tot, off);
+            if (lane >= off) tot += o;
+        }
+        const int total = __shfl_sync(kFull, tot, 31);
+        int run = __shfl_sync(kFull, tot, warp) - warp_tot[warp] + incl - chunk;
+        for (int p = p_lo; p < p_hi; ++p) {  // this thread's own entries
+            const int v = offs[p];
+            offs[p] = run;
+            if (tile == 0) offsets[p] = run;
+            run += v;
+        }
+        if (threadIdx.x == 0) {
+            offs[P] = total;
+            if (tile == 0) offsets[P] = total;
+        }
+    }
+    __syncthreads();
+
+    // Place this tile's copies: slot = offset + tile base + in-tile rank.
+    const int n = T * k;
+    for (int it = threadIdx.x; it < kTileTokens * k; it += kRouteThreads) {
+        const int itl = it / k;
+        const int j = it - itl * k;
+        const int t = tile * kTileTokens + itl;
+        if (t >= T) continue;
+        const int p = sel_p[it];
+        int r = -1;
+        if (p >= 0 && p < P) r = offs[p] + s_base[p] + __popc(mask[p] & ((1u << itl) - 1u));
+        if (r < 0 || r >= n) {
+            set_error(err, MOE_DEVERR_SLOT);
+            slot[(size_t)t * k + j] = -1;
+            continue;
+        }
+        slot[(size_t)t * k + j] = r;
+        src_token[r] = t;
+        src_k[r] = j;
+    }
+    MOE_TRACE_MARK(tr_single, 7);
+    cluster_wait();  // no CTA leaves while another may still read its masks
+}
+
 
 constexpr size_t kTailSmemMax = 96 * 1024;
 size_t tail_smem(size_t route_smem, int P, int n_tiles, int* col_smem);
@@ -615,6 +735,19 @@ cudaError_t launch_single(const float* logits, int T, int E, int P, int k, const
     return launch_pdl_at(urgent, plan_single_kernel<EPL>, dim3(n_tiles), dim3(kRouteThreads), smem1, s, logits, T,
                          E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, counts,
                          offsets, slot, src_token, src_k, err, ticket, col_smem);
+}
+
+template <int EPL>
+cudaError_t launch_cluster(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
+                           const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys, int32_t* counts,
+                           int32_t* offsets, int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err,
+                           size_t smem, int n_tiles, int urgent, cudaStream_t s) {
+    const size_t smem1 = smem + (size_t)(2 * P + 1) * sizeof(int32_t);  // tile bases and offsets
+    cudaError_t e;
+    if ((e = smem_attr(plan_cluster_kernel<EPL>, smem1)) != cudaSuccess) return e;
+    return launch_pdl_cluster(urgent, (unsigned)n_tiles, plan_cluster_kernel<EPL>, dim3(n_tiles),
+                              dim3(kRouteThreads), smem1, s, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates,
+                              phys, counts, offsets, slot, src_token, src_k, err);
 }
 
 template <int EPL, int THREADS>
@@ -698,6 +831,21 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
     // is not stretched by waiting for SM slots.
     const int urgent = most_urgent_priority();
     cudaError_t e;
+    if (ticket != nullptr && n_tiles <= kClusterTiles && cluster_launch_supported()) {
+        const int epl = (E + 31) / 32;
+#define MOE_CLUSTER_CASE(N)                                                                                   \
+    e = launch_cluster<N>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, counts, offsets, slot,     \
+                          src_token, src_k, err, smem, n_tiles, urgent, s)
+        if (epl <= 1) MOE_CLUSTER_CASE(1);
+        else if (epl <= 2) MOE_CLUSTER_CASE(2);
+        else if (epl <= 4) MOE_CLUSTER_CASE(4);
+        else if (epl <= 8) MOE_CLUSTER_CASE(8);
+        else if (epl <= 16) MOE_CLUSTER_CASE(16);
+        else MOE_CLUSTER_CASE(32);
+#undef MOE_CLUSTER_CASE
+        if (e == cudaSuccess) *launches += 1;
+        return e;
+    }
     if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
         const int epl = (E + 31) / 32;
 #define MOE_SINGLE_CASE(N)                                                                                      \

@@ -68,4 +68,31 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) 
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Thread-block clusters.  The CTAs of a cluster are scheduled together, so
+// the cluster barrier is a hardware barrier like __syncthreads (every thread
+// of every CTA of the cluster arrives), not a wait on a flag.  arrive has
+// release semantics and wait acquire semantics at cluster scope: shared-memory
+// writes before the arrive are visible to every CTA after its wait.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+    cluster_arrive();
+    cluster_wait();
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// 32-bit load from the shared memory of CTA `rank` of this cluster, at the
+// address that `local` has in this CTA's shared memory (same layout in every
+// CTA of the cluster).
+__device__ __forceinline__ uint32_t ld_cluster_shared_u32(const void* local, uint32_t rank) {
+    const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t ra, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+    return v;
+}
+
 }  // namespace moe

@@ -30,7 +30,7 @@ KINDS = {
     1: ("column_scan", ["start", "end"]),
     2: ("assign", ["start", "offsets", "end"]),
     3: ("plan_single", ["start", "top-k", "gates(pairs)", "fallback", "replicas+masks", "counts+ranks",
-                        "tail(last)", "end(last)"]),
+                        "handoff", "end"]),
     4: ("dispatch", ["start", "quantized", "slots", "stored"]),
     5: ("combine", ["start", "slots", "accumulated", "stored"]),
 }
