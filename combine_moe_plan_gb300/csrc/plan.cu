@@ -641,9 +641,13 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
     const int p_hi = min(P, p_lo + per);
     int chunk = 0;
     for (int p = p_lo; p < p_hi; ++p) {
+        uint32_t m[kClusterTiles];  // all remote loads in flight before the first use
+#pragma unroll
+        for (int c = 0; c < kClusterTiles; ++c) m[c] = (c < n_cta) ? ld_cluster_shared_u32(mask + p, (uint32_t)c) : 0u;
         int total = 0, before = 0;
-        for (int c = 0; c < n_cta; ++c) {
-            const int cnt = __popc(ld_cluster_shared_u32(mask + p, (uint32_t)c));
+#pragma unroll
+        for (int c = 0; c < kClusterTiles; ++c) {
+            const int cnt = __popc(m[c]);
             before += (c < tile) ? cnt : 0;
             total += cnt;
         }
