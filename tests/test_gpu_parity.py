@@ -448,6 +448,19 @@ def test_plan_path_switch_at_32_tiles():
                 seed=int(rng.integers(1 << 30)), T_max=1025, pool=pool)
 
 
+def test_plan_path_switch_at_8_tiles():
+    """256 tokens (8 tiles) take the cluster plan, 257 (9 tiles) the ticket
+    plan; both on one pool, one after the other, in both orders, with the
+    bench workload's replica map."""
+    rng = np.random.default_rng(13)
+    E, P, k, H = 256, 288, 8, 256
+    inp = wl.make_inputs(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 257))
+    pool = moe.Pool(257, H, E, P, k, n_sets=2)
+    for T in (256, 257, 256, 33, 32):
+        _custom(T, H, E, P, k, inp["logits"][:T], rep_off=inp["rep_off"], rep_ids=inp["rep_ids"],
+                seed=int(rng.integers(1 << 30)), T_max=257, pool=pool)
+
+
 def test_three_launch_plan_at_maximum_shapes():
     """More than 32 tiles (so the route / column-scan / assign kernels run)
     at the largest shapes the API takes: E = 1024, P = 4096 (four replicas per
