@@ -139,7 +139,6 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     }
     const int tl = threadIdx.x / L;  // this segment's token within the tile
     const int sl = threadIdx.x % L;  // lane within the segment
-    const unsigned seg_mask = (L == 32) ? kFull : ((1u << L) - 1u) << ((threadIdx.x & 31) & ~(L - 1));
     const int t0 = tile * kTileTokens;
     const int t = t0 + tl;
 
@@ -152,14 +151,17 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     // after which the winning lane marks the slot taken and promotes its
     // second key (rescanning only when it has none left).  Key 0 sits below
     // every finite logit and marks padding.  Lane j keeps the j-th winner and
-    // its key, whose inverse is the selected logit.
-    if (t < T) {
-        const float* row = logits + (size_t)t * E;
+    // its key, whose inverse is the selected logit.  Every lane runs the
+    // rounds (a token past T has only padding keys and writes nothing), so
+    // the segment butterflies below always see a converged warp.
+    {
+        const bool tok_ok = t < T;
+        const float* row = logits + (size_t)(tok_ok ? t : t0) * E;
         uint32_t key[EPL];
 #pragma unroll
         for (int r = 0; r < EPL; ++r) {
             const int e = r * L + sl;
-            key[r] = (e < E) ? order_key(__ldg(row + e)) : 0u;
+            key[r] = (tok_ok && e < E) ? order_key(__ldg(row + e)) : 0u;
         }
         uint32_t taken = 0u, k1, k2;
         int r1, r2;
@@ -168,8 +170,24 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
         int my_e = 0;
         uint32_t my_key = 0u;
         for (int j = 0; j < k; ++j) {
-            const uint32_t m = __reduce_max_sync(seg_mask, k1);
-            int win = (int)__reduce_min_sync(seg_mask, (k1 == m) ? cand : (uint32_t)INT_MAX);
+            uint32_t m;
+            int win;
+            if (L == 32) {  // whole warp: redux.sync (26 cycles on GB300)
+                m = __reduce_max_sync(kFull, k1);
+                win = (int)__reduce_min_sync(kFull, (k1 == m) ? cand : (uint32_t)INT_MAX);
+            } else {
+                // A segment-masked redux.sync takes about 170 cycles here, so
+                // the segment reduces (key, ~id) packed in 64 bits with one
+                // xor butterfly: the largest key, then the smallest id.
+                uint64_t kv = ((uint64_t)k1 << 32) | (uint64_t)(0xffffffffu - cand);
+#pragma unroll
+                for (int off = L / 2; off > 0; off >>= 1) {
+                    const uint64_t o = __shfl_xor_sync(kFull, kv, off);
+                    kv = o > kv ? o : kv;
+                }
+                m = (uint32_t)(kv >> 32);
+                win = (int)(0xffffffffu - (uint32_t)kv);
+            }
             if (win >= E) win = 0;  // only reachable with NaN logits (outside the domain)
             if (sl == (win & (L - 1))) {
                 taken |= 1u << r1;
@@ -187,7 +205,7 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
                 my_key = m;
             }
         }
-        if (sl < k) {
+        if (tok_ok && sl < k) {
             sel_v[tl * k + sl] = key_value(my_key);
             sel_e[tl * k + sl] = my_e;
         }
