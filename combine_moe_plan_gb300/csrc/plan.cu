@@ -865,8 +865,14 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
         else if (epl <= 16) MOE_CLUSTER_CASE(16);
         else MOE_CLUSTER_CASE(32);
 #undef MOE_CLUSTER_CASE
-        if (e == cudaSuccess) *launches += 1;
-        return e;
+        if (e == cudaSuccess) {
+            *launches += 1;
+            return e;
+        }
+        // A cluster this size that cannot be placed is a launch-time error
+        // (nothing was enqueued and the context stays usable): clear it and
+        // use the ticket kernel instead.
+        (void)cudaGetLastError();
     }
     if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
         const int epl = (E + 31) / 32;
