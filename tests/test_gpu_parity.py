@@ -284,10 +284,12 @@ def test_launch_count():
     _check_all(big, inp, Run(big, inp, pool=pool))
 
 
-def test_step_captures_in_a_cuda_graph():
+@pytest.mark.parametrize("T", [96, 512])
+def test_step_captures_in_a_cuda_graph(T):
     """plan -> dispatch -> combine (PDL launches) captured once in a CUDA graph
-    and replayed on new input contents gives the oracle's results."""
-    w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 512)
+    and replayed on new input contents gives the oracle's results: 96 tokens
+    (the cluster plan) and 512 (the ticket plan)."""
+    w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T)
     pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
     inp0 = wl.make_inputs(w, seed=0)
     logits, x, ex = dev(inp0["logits"]), dev_bf16(inp0["x"]), dev_bf16(inp0["ex_out"])
