@@ -202,7 +202,10 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     const bool item_ok = itl < kTileTokens && ij < k && t0 + itl < T;
     float g = 0.0f;
     bool slow = false;
-    {
+    // Only the first 32 kp threads hold items; the other warps (a multiple of
+    // 32 threads, so whole warps) skip the stage.
+    const bool gate_warp = (int)threadIdx.x < kTileTokens * kp;
+    if (gate_warp) {
         dword::dw e = {0.0f, 0.0f};
         if (item_ok) {
             const dword::dw d = dword::two_sum(sel_v[it], -sel_v[itl * k]);
@@ -225,7 +228,7 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
         }
     }
     ROUTE_MARK(2);
-    const unsigned slow_lanes = __ballot_sync(kFull, slow);
+    const unsigned slow_lanes = gate_warp ? __ballot_sync(kFull, slow) : 0u;
     if (slow_lanes != 0u) {  // warp-uniform; rare
         const int seg = (int)(threadIdx.x & 31) & ~(kp - 1);
         const unsigned seg_bits = (kp == 32 ? 0xffffffffu : ((1u << kp) - 1u)) << seg;
