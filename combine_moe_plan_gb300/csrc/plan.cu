@@ -363,7 +363,8 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
 // offsets), and places its own tile's copies.  No ticket, no single-CTA tail,
 // no global tile counts or ranks.  Trace stages 0-5 as route_tile; 6 cluster
 // barrier passed, 7 copies placed.
-constexpr int kClusterTiles = 8;  // the portable cluster size
+constexpr int kClusterTiles = 16;        // the largest cluster Blackwell schedules
+constexpr int kClusterPortableTiles = 8;  // larger clusters need the non-portable attribute
 
 template <int EPL>
 __global__ void __launch_bounds__(kRouteThreads)
@@ -509,6 +510,10 @@ cudaError_t launch_cluster(const float* logits, int T, int E, int P, int k, cons
     const size_t smem1 = smem + (size_t)(2 * P + 1) * sizeof(int32_t);  // tile bases and offsets
     cudaError_t e;
     if ((e = smem_attr(plan_cluster_kernel<EPL>, smem1)) != cudaSuccess) return e;
+    if (n_tiles > kClusterPortableTiles &&
+        (e = cudaFuncSetAttribute(plan_cluster_kernel<EPL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
+            cudaSuccess)
+        return e;
     return launch_pdl_cluster(urgent, (unsigned)n_tiles, plan_cluster_kernel<EPL>, dim3(n_tiles),
                               dim3(kRouteThreads), smem1, s, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates,
                               phys, counts, offsets, slot, src_token, src_k, err);

@@ -284,11 +284,11 @@ def test_launch_count():
     _check_all(big, inp, Run(big, inp, pool=pool))
 
 
-@pytest.mark.parametrize("T", [96, 512])
+@pytest.mark.parametrize("T", [96, 512, 1000])
 def test_step_captures_in_a_cuda_graph(T):
     """plan -> dispatch -> combine (PDL launches) captured once in a CUDA graph
-    and replayed on new input contents gives the oracle's results: 96 tokens
-    (the cluster plan) and 512 (the ticket plan)."""
+    and replayed on new input contents gives the oracle's results: 96 and 512
+    tokens (the cluster plan, portable and 16-CTA) and 1000 (the ticket plan)."""
     w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T)
     pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
     inp0 = wl.make_inputs(w, seed=0)
@@ -450,17 +450,18 @@ def test_plan_path_switch_at_32_tiles():
                 seed=int(rng.integers(1 << 30)), T_max=1025, pool=pool)
 
 
-def test_plan_path_switch_at_8_tiles():
-    """256 tokens (8 tiles) take the cluster plan, 257 (9 tiles) the ticket
-    plan; both on one pool, one after the other, in both orders, with the
-    bench workload's replica map."""
+def test_plan_path_switch_at_cluster_sizes():
+    """Up to 8 tiles the cluster plan is portable, 9 to 16 tiles need the
+    non-portable cluster size, 17 tiles and more take the ticket plan: 256,
+    257, 512 and 513 tokens on one pool, one after the other, in both orders,
+    with the bench workload's replica map."""
     rng = np.random.default_rng(13)
     E, P, k, H = 256, 288, 8, 256
-    inp = wl.make_inputs(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 257))
-    pool = moe.Pool(257, H, E, P, k, n_sets=2)
-    for T in (256, 257, 256, 33, 32):
+    inp = wl.make_inputs(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 513))
+    pool = moe.Pool(513, H, E, P, k, n_sets=2)
+    for T in (256, 257, 512, 513, 512, 257, 33, 32):
         _custom(T, H, E, P, k, inp["logits"][:T], rep_off=inp["rep_off"], rep_ids=inp["rep_ids"],
-                seed=int(rng.integers(1 << 30)), T_max=257, pool=pool)
+                seed=int(rng.integers(1 << 30)), T_max=513, pool=pool)
 
 
 def test_three_launch_plan_at_maximum_shapes():
