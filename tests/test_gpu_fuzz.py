@@ -20,10 +20,13 @@ def _built():
 
 
 def _random_case(rng):
-    T = int(rng.choice([1, 2, 31, 32, 33, 95, 257, 700, 1500]))
+    # batch sizes on both sides of every plan form's limit (1 tile; 8 and 16
+    # tiles for the cluster plan; 32 for the ticket plan) and beyond
+    T = int(rng.choice([1, 2, 31, 32, 33, 95, 256, 257, 512, 513, 700, 1024, 1025, 1500]))
     H = int(rng.choice([128, 256, 384, 896, 2048]))
     E = int(rng.integers(1, 300))
-    k = int(rng.integers(1, min(E, 12) + 1))
+    k_max = 32 if rng.random() < 0.25 else 12
+    k = int(rng.integers(1, min(E, k_max) + 1))
     n_rep = int(rng.integers(0, min(E, 40) + 1)) if rng.random() < 0.6 else 0
     P = E + n_rep
     rep_off = rep_ids = None
