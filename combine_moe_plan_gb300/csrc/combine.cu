@@ -34,8 +34,11 @@ combine_kernel(const uint16_t* __restrict__ ex_out, const int32_t* __restrict__ 
                int32_t* __restrict__ err) {
     // Trace stages (warp 0 of the CTA): 0 start, 1 slots and gates loaded,
     // 2 accumulation done, 3 output stored.
+    // No early launch_dependents: the kernel after combine is normally the
+    // next batch's plan, whose CTAs would sit on SMs in their wait while this
+    // grid streams.  Letting dependents start only at exit measured 1 us
+    // shorter per pipelined 4096-token step (124.3 vs 125.3 us).
     grid_dependency_sync();
-    allow_dependents();
     MOE_TRACE_SM(tr_combine);
     MOE_TRACE_MARK(tr_combine, 0);
     const int lane = threadIdx.x & 31;

@@ -31,8 +31,6 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32
                 int8_t* __restrict__ codes, float* __restrict__ scales, int Gs, int32_t* __restrict__ err) {
     // Trace stages (warp 0 of the CTA): 0 start, 1 quantized, 2 slots read,
     // 3 stores issued.
-    grid_dependency_sync();
-    allow_dependents();
     MOE_TRACE_SM(tr_dispatch);
     MOE_TRACE_MARK(tr_dispatch, 0);
     const int lane = threadIdx.x & 31;
@@ -42,10 +40,22 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32
     const int seg = (int)(item - (long long)t * segs);
     if (t >= T) return;
 
+    // x is loaded and quantized before the wait for the previous kernel.  That
+    // kernel is the plan, which does not write x and lets its dependents start
+    // only after its own wait has returned, i.e. once everything before it on
+    // the stream has completed and its writes are visible; so x is final here.
+    // include/moe.h makes this a precondition of moe_dispatch (the kernel
+    // launched just before it must not write x and must let its dependents
+    // start only after its own wait).  The slots come from the
+    // plan: read after the wait.  Dependents may start only after the wait, as
+    // in every kernel of the library, so that whatever runs next on the stream
+    // sees all writes made before this kernel.
     const SegLoad ld = load_segment(x, t, H, seg, lane);
-    const int my_slot = (lane < k) ? slot[(size_t)t * k + lane] : 0;
     const SegQuant qz = quantize_segment(ld);
     MOE_TRACE_MARK(tr_dispatch, 1);
+    grid_dependency_sync();
+    allow_dependents();
+    const int my_slot = (lane < k) ? slot[(size_t)t * k + lane] : 0;
     MOE_TRACE_MARK(tr_dispatch, 2);
     store_segment(ld, qz, my_slot, k, T * k, H, Gs, seg, codes, scales, err);
     MOE_TRACE_MARK(tr_dispatch, 3);

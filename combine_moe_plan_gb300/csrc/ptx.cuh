@@ -47,9 +47,10 @@ __device__ __forceinline__ void set_error(int32_t* err, int bits) { atomicOr(err
 
 
 // Programmatic dependent launch.  Every kernel of the library calls
-// grid_dependency_sync() before its first global-memory access: it returns once
-// the preceding kernel in the stream has completed and its writes are visible
-// (immediately if there is none).  allow_dependents() then lets the next
+// grid_dependency_sync() before its first access to memory that the preceding
+// kernel may write: it returns once that kernel has completed and its writes
+// are visible (immediately if there is none).  Dispatch reads x, which its
+// preceding kernel (the plan) never writes, before the call.  allow_dependents() then lets the next
 // kernel's CTAs be scheduled while this grid drains; they park in their own
 // grid_dependency_sync(), so ordering is unchanged -- only launch latency is
 // hidden.

@@ -34,6 +34,17 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *     work is asynchronous on that stream; nothing synchronizes except
  *     moe_pool_check and moe_step_host's documented copies.
+ *   - Kernels are launched with programmatic dependent launch: each may start
+ *     while the kernel before it on the stream drains, and waits for it
+ *     (griddepcontrol.wait) before reading what it may have written; each
+ *     lets its own dependents start only after that wait.  The one exception
+ *     is moe_dispatch, which reads x before its wait.  So the kernel launched
+ *     immediately before moe_dispatch on `stream` must not write x, and if
+ *     that kernel was itself launched with programmatic dependent launch it
+ *     must let its dependents start only after its own wait.  Every kernel of
+ *     this library meets the second condition; moe_plan, the usual
+ *     predecessor, also never writes x.  Writes by anything earlier in stream
+ *     order, or by a memory copy right before moe_dispatch, are seen.
  *   - The caller owns every buffer, including the pool workspace; the library
  *     never allocates device memory.
  *   - Inputs outside the documented domain (non-finite logits or activations,
@@ -183,6 +194,9 @@ MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T,
  * code = rint((x * 127) / amax) in fp32, half-even (amax = 0: scale 0, codes 0).
  * Row slot[t, j] of codes / scales receives token t's codes / scales for every
  * j.  Requires a prior moe_plan on this set with the same T (T = 0: no-op).
+ * x is read before the wait for the preceding kernel: the kernel launched
+ * just before this call on `stream` must not write x and must not let its
+ * dependents start before its own wait (see the conventions).
  */
 MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream);
 

@@ -512,3 +512,66 @@ def test_bench_schedule_two_streams_full_size():
         np.testing.assert_array_equal(v["slot"].cpu().numpy(), pl["slot"])
         codes, _ = oracle.dispatch(inp["x"], pl["slot"])
         np.testing.assert_array_equal(v["codes"][:w.rows].cpu().numpy(), codes)
+
+
+@pytest.mark.parametrize("name,T", [("t96_h7168_e256_k8", 96), ("t4096_h7168_e256p288_k8", 300),
+                                    ("t16384_h2048_e64_k6", 1000), ("t16384_h2048_e64_k6", 2000)])
+def test_layers_chained_on_one_stream(name, T):
+    """Six layers back to back on one stream, each layer's y the next layer's x,
+    the two buffer sets alternating, no synchronization in between; then the
+    same chain captured once as a CUDA graph and replayed.  Every layer's y
+    equals the oracle run layer after layer on its own outputs.  Dispatch reads
+    x before its wait for the plan, so this checks that the previous layer's
+    combine has finished writing x by then (the plan in between waits for it).
+    The plan forms covered: cluster (96, 300 tokens), one launch (1000), three
+    launches (2000)."""
+    w = wl.small_variant(wl.WORKLOADS[name], T)
+    L = 6
+    layers = [wl.make_inputs(w, seed=10 + l, with_expert_out=False) for l in range(L)]
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
+    x0 = dev_bf16(layers[0]["x"])
+    lg = [dev(inp["logits"]) for inp in layers]
+    ro = [None if inp["rep_off"] is None else dev(inp["rep_off"]) for inp in layers]
+    ri = [None if inp["rep_ids"] is None else dev(inp["rep_ids"]) for inp in layers]
+    ys = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+
+    refs, x = [], layers[0]["x"]
+    for l, inp in enumerate(layers):
+        refs.append(oracle.forward(inp["logits"], x, w.k, inp["rep_off"], inp["rep_ids"], w.P)["y"])
+        x = refs[-1]
+
+    s = torch.cuda.Stream()
+
+    def chain():
+        xin = x0
+        for l in range(L):
+            b = l & 1
+            pool.plan(lg[l], ro[l], ri[l], buf=b, stream=s)
+            pool.dispatch(xin, buf=b, stream=s)
+            pool.identity_experts(w.T, buf=b, stream=s)
+            pool.combine(w.T, y=ys[l], buf=b, stream=s)
+            xin = ys[l]
+
+    def fill_nan():
+        for y in ys:
+            y.view(torch.int16).fill_(-1)  # 0xffff: a NaN that no layer produces
+        torch.cuda.synchronize()
+
+    fill_nan()
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert_y_close(host_u16(ys[l]), refs[l], f"{name} T={T} layer {l}")
+    assert pool.check() == 0
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    for _ in range(2):
+        fill_nan()
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(L):
+            assert_y_close(host_u16(ys[l]), refs[l], f"{name} T={T} graph layer {l}")
+    assert pool.check() == 0
