@@ -38,6 +38,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -75,18 +76,43 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback (earlier GB300 copy measurement)"
 
 
+CSRC = os.path.join(ROOT, "combine_moe_plan_gb300", "csrc")
+
+
+def source_closure(kernel_file: str) -> list:
+    """The kernel's source file and every csrc file it includes with
+    #include "...", transitively, sorted by name."""
+    seen, todo = set(), [kernel_file]
+    while todo:
+        f = todo.pop()
+        if f in seen or not os.path.exists(os.path.join(CSRC, f)):
+            continue
+        seen.add(f)
+        for line in open(os.path.join(CSRC, f), encoding="utf-8"):
+            m = re.match(r'\s*#\s*include\s+"([^"]+)"', line)
+            if m:
+                todo.append(m.group(1))
+    return sorted(seen)
+
+
+def source_hash(kernel_file: str) -> str:
+    """sha256 over (name, contents) of the kernel's source closure."""
+    h = hashlib.sha256()
+    for f in source_closure(kernel_file):
+        h.update(f.encode() + b"\0")
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()
+
+
 def _traffic(kernel_file: str, kernel: str):
     """Per-launch DRAM bytes from a committed ncu summary, if the kernel's
-    source has not changed since it was captured."""
+    source (with everything it includes) has not changed since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f).get(kernel)
-    if not d:
-        return None
-    src = open(os.path.join(ROOT, "combine_moe_plan_gb300", "csrc", kernel_file), "rb").read()
-    if hashlib.sha256(src).hexdigest() != d.get("source_sha256"):
+    if not d or source_hash(kernel_file) != d.get("source_sha256"):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -267,8 +293,9 @@ class _Streams:
 def _graph_per_op(torch, pool, logits, rep_off, rep_ids, x, y, T, reps=200, warm=10) -> dict:
     """Each op of one step on buffer set 0 captured as its own CUDA graph and
     replayed `reps` times after `warm` untimed replays: GPU time per replay
-    (CUDA events around it) as [p10, median, p90] in microseconds.  "dispatch"
-    is plan + dispatch: the routing metadata belongs to the fused dispatch."""
+    (CUDA events around it) as [p10, median, p90] in microseconds.
+    "plan+dispatch" is one graph of both: the routing metadata belongs to the
+    fused dispatch."""
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         pool.plan(logits, rep_off, rep_ids, buf=0, stream=s)
@@ -284,7 +311,7 @@ def _graph_per_op(torch, pool, logits, rep_off, rep_ids, x, y, T, reps=200, warm
 
     graphs = {
         "plan": capture(lambda: pool.plan(logits, rep_off, rep_ids, buf=0, stream=s)),
-        "dispatch": capture(lambda: (pool.plan(logits, rep_off, rep_ids, buf=0, stream=s),
+        "plan+dispatch": capture(lambda: (pool.plan(logits, rep_off, rep_ids, buf=0, stream=s),
                                      pool.dispatch(x, buf=0, stream=s))),
         "combine": capture(lambda: pool.combine(T, y=y, buf=0, stream=s)),
     }

@@ -83,3 +83,17 @@ def test_cpu_baseline_reports_all_cores_and_single_thread():
     assert d["cores"] == oracle.threads() >= 1
     assert d["single_thread"]["cores"] == 1 and d["single_thread"]["value"] > 0
     oracle.set_threads(before)
+
+
+def test_traffic_follows_the_kernel_source_closure(monkeypatch):
+    """The ncu traffic figure is keyed to a hash over the kernel file and every
+    csrc header it includes: a change to any of them drops the figure."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert {"combine.cu", "ptx.cuh", "moe_internal.h"} <= set(bench.source_closure("combine.cu"))
+    assert "quant.cuh" in bench.source_closure("dispatch.cu")
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["combine_kernel"]
+    monkeypatch.setattr(bench, "source_hash", lambda f: rec["source_sha256"])
+    assert bench._traffic("combine.cu", "combine_kernel") == rec["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "source_hash", lambda f: "0" * 64)
+    assert bench._traffic("combine.cu", "combine_kernel") is None
