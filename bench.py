@@ -104,15 +104,17 @@ def source_hash(kernel_file: str) -> str:
     return h.hexdigest()
 
 
-def _traffic(kernel_file: str, kernel: str):
-    """Per-launch DRAM bytes from a committed ncu summary, if the kernel's
-    source (with everything it includes) has not changed since the capture."""
+def _traffic(kernel_file: str, kernel: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary: only for the
+    workload it was captured on, and only if the kernel's source (with
+    everything it includes) has not changed since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f).get(kernel)
-    if not d or source_hash(kernel_file) != d.get("source_sha256"):
+        rec = json.load(f)
+    d = rec.get(kernel)
+    if not d or rec.get("workload") != workload or source_hash(kernel_file) != d.get("source_sha256"):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -521,7 +523,7 @@ def run_ours(a, w: wl.Workload):
         bytes_ = w.algorithmic_bytes()
         peak, peak_src = _peaks()
         achieved = bytes_["combine"] / (b2b_us["combine"] * 1e-6) / 1e9
-        traffic = _traffic("combine.cu", "combine_kernel")
+        traffic = _traffic("combine.cu", "combine_kernel", w.name)
         tokens = w.T * ws
         out = {
             "metric": "dispatch+combine tokens/s (plan+dispatch+combine per step)",

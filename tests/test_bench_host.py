@@ -86,14 +86,18 @@ def test_cpu_baseline_reports_all_cores_and_single_thread():
 
 
 def test_traffic_follows_the_kernel_source_closure(monkeypatch):
-    """The ncu traffic figure is keyed to a hash over the kernel file and every
-    csrc header it includes: a change to any of them drops the figure."""
+    """The ncu traffic figure is keyed to its workload and to a hash over the
+    kernel file and every csrc header it includes: another workload, or a
+    change to any of those files, drops the figure."""
     sys.path.insert(0, ROOT)
     import bench
     assert {"combine.cu", "ptx.cuh", "moe_internal.h"} <= set(bench.source_closure("combine.cu"))
     assert "quant.cuh" in bench.source_closure("dispatch.cu")
-    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["combine_kernel"]
+    top = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    rec, wname = top["combine_kernel"], top["workload"]
     monkeypatch.setattr(bench, "source_hash", lambda f: rec["source_sha256"])
-    assert bench._traffic("combine.cu", "combine_kernel") == rec["dram_bytes_per_launch"]
+    assert bench._traffic("combine.cu", "combine_kernel", wname) == rec["dram_bytes_per_launch"]
+    # a per-launch figure belongs to the workload it was captured on
+    assert bench._traffic("combine.cu", "combine_kernel", "t96_h7168_e256_k8") is None
     monkeypatch.setattr(bench, "source_hash", lambda f: "0" * 64)
-    assert bench._traffic("combine.cu", "combine_kernel") is None
+    assert bench._traffic("combine.cu", "combine_kernel", wname) is None
