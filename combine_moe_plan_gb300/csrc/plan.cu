@@ -355,8 +355,14 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
 }
 
 // Batches of at most kClusterTiles tiles (the decode regime), launched as one
-// thread-block cluster of one CTA per tile.  Every CTA routes its tile (the
-// route_tile body) and keeps its per-expert token masks in shared memory;
+// thread-block cluster of one CTA per tile of TT tokens: the smallest of 8,
+// 16 and 32 that keeps the cluster within the portable 8 CTAs (8 up to 64
+// tokens, 16 up to 128), else 32 (up to 16 CTAs).  A CTA routes one token per
+// warp, and 32 warps routing at once on one SM take about twice as long per
+// arg-max round as eight, so a small batch is spread over more SMs; larger
+// clusters of small tiles plan faster from an idle GPU but wait for SMs when
+// another stream's kernels fill the GPU.  Every CTA routes its tile
+// (the route_tile body) and keeps its per-expert token masks in shared memory;
 // after the cluster barrier each CTA reads every tile's masks over
 // distributed shared memory, so it knows, per physical expert, the copies in
 // earlier tiles (its tile base) and in all tiles (the counts, scanned into the
@@ -366,27 +372,28 @@ plan_single_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
 constexpr int kClusterTiles = 16;        // the largest cluster Blackwell schedules
 constexpr int kClusterPortableTiles = 8;  // larger clusters need the non-portable attribute
 
-template <int EPL>
-__global__ void __launch_bounds__(kRouteThreads)
+template <int EPL, int TT>
+__global__ void __launch_bounds__(32 * TT)
 plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
                     const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
                     int32_t* __restrict__ topk_e, float* __restrict__ gates, int32_t* __restrict__ phys,
                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
                     int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err) {
+    constexpr int THREADS = 32 * TT;  // one warp per token
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ int32_t warp_tot[kRouteThreads / 32];
+    __shared__ int32_t warp_tot[TT];
     grid_dependency_sync();
     allow_dependents();
     MOE_TRACE_SM(tr_single);
     const int tile = (int)cluster_ctarank();  // the grid is one cluster
-    route_tile<EPL, kRouteInCluster, kRouteThreads>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
-                                                    nullptr, (int)gridDim.x, nullptr, err, smem, tile);
+    route_tile<EPL, kRouteInCluster, THREADS, TT>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
+                                                  nullptr, (int)gridDim.x, nullptr, err, smem, tile);
     // route_tile's shared-memory layout: exp table, sel_v, sel_e, sel_p [32k],
     // masks [P], replica offsets [E+1] and ids [P]; then this kernel's arrays.
     const int32_t* sel_p = reinterpret_cast<const int32_t*>(
                                reinterpret_cast<float2*>(smem) + 2 * dword::kExpTableHalf + 1) +
-                           2 * kTileTokens * k;
-    const uint32_t* mask = reinterpret_cast<const uint32_t*>(sel_p + kTileTokens * k);
+                           2 * TT * k;
+    const uint32_t* mask = reinterpret_cast<const uint32_t*>(sel_p + TT * k);
     int32_t* s_base = const_cast<int32_t*>(reinterpret_cast<const int32_t*>(mask + P)) + (E + 1) + P;  // [P]
     int32_t* offs = s_base + P;                                                                         // [P+1]
 
@@ -397,7 +404,7 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
     // thread takes a contiguous chunk of experts and keeps its chunk's total
     // in a register for the scan into offsets.
     const int n_cta = (int)gridDim.x;
-    const int per = (P + kRouteThreads - 1) / kRouteThreads;
+    const int per = (P + THREADS - 1) / THREADS;
     const int p_lo = threadIdx.x * per;
     const int p_hi = min(P, p_lo + per);
     int chunk = 0;
@@ -431,8 +438,7 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
         }
         if (lane == 31) warp_tot[warp] = incl;
         __syncthreads();
-        static_assert(kRouteThreads == 32 * 32, "one warp total per lane");
-        int tot = warp_tot[lane];
+        int tot = lane < TT ? warp_tot[lane] : 0;  // TT warps, one total each
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int o = __shfl_up_sync(kFull, tot, off);
@@ -455,10 +461,10 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
 
     // Place this tile's copies: slot = offset + tile base + in-tile rank.
     const int n = T * k;
-    for (int it = threadIdx.x; it < kTileTokens * k; it += kRouteThreads) {
+    for (int it = threadIdx.x; it < TT * k; it += THREADS) {
         const int itl = it / k;
         const int j = it - itl * k;
-        const int t = tile * kTileTokens + itl;
+        const int t = tile * TT + itl;
         if (t >= T) continue;
         const int p = sel_p[it];
         int r = -1;
@@ -502,21 +508,41 @@ cudaError_t launch_single(const float* logits, int T, int E, int P, int k, const
                          offsets, slot, src_token, src_k, err, ticket, col_smem);
 }
 
-template <int EPL>
+// Dynamic shared memory of route_tile for tiles of `tt` tokens: exp table,
+// sel_v / sel_e / sel_p [tt k], masks [P], replica offsets [E+1] and ids [P].
+size_t route_smem(int tt, int E, int P, int k) {
+    return (2 * dword::kExpTableHalf + 1) * sizeof(float2) +
+           (size_t)tt * k * (sizeof(float) + 2 * sizeof(int32_t)) + (size_t)P * sizeof(uint32_t) +
+           (size_t)(E + 1 + P) * sizeof(int32_t);
+}
+
+template <int EPL, int TT>
 cudaError_t launch_cluster(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
                            const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys, int32_t* counts,
                            int32_t* offsets, int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err,
-                           size_t smem, int n_tiles, int urgent, cudaStream_t s) {
-    const size_t smem1 = smem + (size_t)(2 * P + 1) * sizeof(int32_t);  // tile bases and offsets
+                           int urgent, cudaStream_t s) {
+    const int n_tiles = (T + TT - 1) / TT;
+    const size_t smem1 = route_smem(TT, E, P, k) + (size_t)(2 * P + 1) * sizeof(int32_t);  // + tile bases, offsets
     cudaError_t e;
-    if ((e = smem_attr(plan_cluster_kernel<EPL>, smem1)) != cudaSuccess) return e;
+    if ((e = smem_attr(plan_cluster_kernel<EPL, TT>, smem1)) != cudaSuccess) return e;
     if (n_tiles > kClusterPortableTiles &&
-        (e = cudaFuncSetAttribute(plan_cluster_kernel<EPL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
-            cudaSuccess)
+        (e = cudaFuncSetAttribute(plan_cluster_kernel<EPL, TT>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                  1)) != cudaSuccess)
         return e;
-    return launch_pdl_cluster(urgent, (unsigned)n_tiles, plan_cluster_kernel<EPL>, dim3(n_tiles),
-                              dim3(kRouteThreads), smem1, s, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates,
-                              phys, counts, offsets, slot, src_token, src_k, err);
+    return launch_pdl_cluster(urgent, (unsigned)n_tiles, plan_cluster_kernel<EPL, TT>, dim3(n_tiles),
+                              dim3(32 * TT), smem1, s, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
+                              counts, offsets, slot, src_token, src_k, err);
+}
+
+// The cluster plan with tiles of TT tokens for `epl` keys a lane.
+template <int TT, typename... A>
+cudaError_t launch_cluster_epl(int epl, A... a) {
+    if (epl <= 1) return launch_cluster<1, TT>(a...);
+    if (epl <= 2) return launch_cluster<2, TT>(a...);
+    if (epl <= 4) return launch_cluster<4, TT>(a...);
+    if (epl <= 8) return launch_cluster<8, TT>(a...);
+    if (epl <= 16) return launch_cluster<16, TT>(a...);
+    return launch_cluster<32, TT>(a...);
 }
 
 template <int EPL, int THREADS>
@@ -588,10 +614,7 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
                         int32_t* tile_hist, int32_t* local_rank, int32_t* counts, int32_t* offsets,
                         int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* err, int32_t* ticket,
                         cudaStream_t s, uint64_t* launches) {
-    const size_t items = (size_t)kTileTokens * k;
-    const size_t smem = (2 * dword::kExpTableHalf + 1) * sizeof(float2) +
-                        items * (sizeof(float) + 2 * sizeof(int32_t)) + (size_t)P * sizeof(uint32_t) +
-                        (size_t)(E + 1 + P) * sizeof(int32_t);
+    const size_t smem = route_smem(kTileTokens, E, P, k);
     const int n_tiles = (T + kTileTokens - 1) / kTileTokens;
     // The plan is latency-bound and on its stream's critical path; bandwidth-
     // bound kernels of other streams (the other buffer set's dispatch and
@@ -601,17 +624,18 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
     const int urgent = most_urgent_priority();
     cudaError_t e;
     if (ticket != nullptr && n_tiles <= kClusterTiles && cluster_launch_supported()) {
+        // The smallest tile that keeps the cluster portable (at most 8 CTAs);
+        // 32-token tiles beyond that, in up to kClusterTiles CTAs.
         const int epl = (E + 31) / 32;
-#define MOE_CLUSTER_CASE(N)                                                                                   \
-    e = launch_cluster<N>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, counts, offsets, slot,     \
-                          src_token, src_k, err, smem, n_tiles, urgent, s)
-        if (epl <= 1) MOE_CLUSTER_CASE(1);
-        else if (epl <= 2) MOE_CLUSTER_CASE(2);
-        else if (epl <= 4) MOE_CLUSTER_CASE(4);
-        else if (epl <= 8) MOE_CLUSTER_CASE(8);
-        else if (epl <= 16) MOE_CLUSTER_CASE(16);
-        else MOE_CLUSTER_CASE(32);
-#undef MOE_CLUSTER_CASE
+        if (T <= 8 * kClusterPortableTiles)
+            e = launch_cluster_epl<8>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, counts,
+                                      offsets, slot, src_token, src_k, err, urgent, s);
+        else if (T <= 16 * kClusterPortableTiles)
+            e = launch_cluster_epl<16>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, counts,
+                                       offsets, slot, src_token, src_k, err, urgent, s);
+        else
+            e = launch_cluster_epl<32>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, counts,
+                                       offsets, slot, src_token, src_k, err, urgent, s);
         if (e == cudaSuccess) {
             *launches += 1;
             return e;

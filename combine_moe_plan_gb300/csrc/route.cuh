@@ -73,13 +73,15 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
-// Route one 32-token tile (the body shared by both plan variants) with a CTA
-// of THREADS = 32 L threads: each token's top-k runs on a segment of L lanes
-// (L = 32: a whole warp; 16 or 8 when the experts fit in at most 8 keys a
-// lane, so that small expert counts do not occupy a whole warp per token).
+// Route one tile of TT tokens (the body every plan kernel runs per CTA) with
+// a CTA of THREADS = TT L threads: each token's top-k runs on a segment of L
+// lanes (L = 32: a whole warp; 16 or 8 when the experts fit in at most 8 keys
+// a lane, so that small expert counts do not occupy a whole warp per token).
+// Tiles are 32 tokens (one mask word) except in the cluster plan, which
+// spreads a small batch over more SMs with tiles of 8 or 16 tokens.
 // Trace stages: 0 start, 1 top-k done, 2 gates from pairs done, 3 fp64
 // fallback done, 4 replicas and masks done, 5 tile counts and ranks written.
-template <int EPL, int WHERE, int THREADS>  // EPL = logits per lane = ceil(E / L)
+template <int EPL, int WHERE, int THREADS, int TT = kTileTokens>  // EPL = logits per lane = ceil(E / L)
 __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int T, int E, int P, int k,
                                            const int32_t* __restrict__ rep_off,
                                            const int32_t* __restrict__ rep_ids, int32_t* __restrict__ topk_e,
@@ -87,13 +89,14 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
                                            int32_t* __restrict__ tile_hist, int n_tiles,
                                            int32_t* __restrict__ local_rank, int32_t* __restrict__ err,
                                            unsigned char* smem, int tile) {
-    constexpr int L = THREADS / 32;  // lanes per token
+    constexpr int L = THREADS / TT;  // lanes per token
     static_assert(L == 8 || L == 16 || L == 32, "8, 16 or 32 lanes per token");
+    static_assert(TT == 8 || TT == 16 || TT == 32, "8, 16 or 32 tokens per tile (bits of a mask word)");
     float2* s_exp = reinterpret_cast<float2*>(smem);                             // exp(m / 512) table
-    float* sel_v = reinterpret_cast<float*>(s_exp + 2 * dword::kExpTableHalf + 1);  // [32*k]
-    int32_t* sel_e = reinterpret_cast<int32_t*>(sel_v + kTileTokens * k);  // [32*k]
-    int32_t* sel_p = sel_e + kTileTokens * k;                               // [32*k]
-    uint32_t* mask = reinterpret_cast<uint32_t*>(sel_p + kTileTokens * k);  // [P]
+    float* sel_v = reinterpret_cast<float*>(s_exp + 2 * dword::kExpTableHalf + 1);  // [TT*k]
+    int32_t* sel_e = reinterpret_cast<int32_t*>(sel_v + TT * k);  // [TT*k]
+    int32_t* sel_p = sel_e + TT * k;                               // [TT*k]
+    uint32_t* mask = reinterpret_cast<uint32_t*>(sel_p + TT * k);  // [P]
     int32_t* s_off = reinterpret_cast<int32_t*>(mask + P);                 // [E+1] replica CSR
     int32_t* s_ids = s_off + (E + 1);                                       // [P]
 
@@ -109,7 +112,7 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     }
     const int tl = threadIdx.x / L;  // this segment's token within the tile
     const int sl = threadIdx.x % L;  // lane within the segment
-    const int t0 = tile * kTileTokens;
+    const int t0 = tile * TT;
     const int t = t0 + tl;
 
     // ---- top-k of token t: k rounds of segment arg-max, ties -> lower id ----
@@ -195,16 +198,17 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     // quotient.  A token with an item the pairs cannot decide, or with
     // l_j - l_0 < -64, is redone in fp64 as e_j = exp(d) with e_0 = 1,
     // s = sum over j ascending and g_j = (float)(e_j / s). ----
-    const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));  // 32 kp <= THREADS (host's choice of L)
+    const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));  // TT kp <= THREADS (host's choice of L)
     const int itl = (int)threadIdx.x / kp;  // token within the tile (>= 32: no item)
     const int ij = (int)threadIdx.x - itl * kp;
     const int it = itl * k + ij;
-    const bool item_ok = itl < kTileTokens && ij < k && t0 + itl < T;
+    const bool item_ok = itl < TT && ij < k && t0 + itl < T;
     float g = 0.0f;
     bool slow = false;
-    // Only the first 32 kp threads hold items; the other warps (a multiple of
-    // 32 threads, so whole warps) skip the stage.
-    const bool gate_warp = (int)threadIdx.x < kTileTokens * kp;
+    // Only the first TT kp threads hold items; warps past them skip the stage.
+    // The test is per warp (TT kp may be below 32), so a warp that enters
+    // enters whole and its full-mask shuffles see every lane.
+    const bool gate_warp = ((int)threadIdx.x & ~31) < TT * kp;
     if (gate_warp) {
         dword::dw e = {0.0f, 0.0f};
         if (item_ok) {

@@ -70,7 +70,8 @@ def summarize(kind: int, n_ctas: int) -> dict:
     name, stages = KINDS[kind]
     st, sm = read(kind)
     ns = st[:n_ctas, :, 0].astype(np.int64)
-    out = {"kernel": name, "ctas": int(n_ctas), "sms": int(len(np.unique(sm[:n_ctas]))), "stages": {}}
+    ran = ns[:, 0] > 0  # the stamps are cleared before each pass
+    out = {"kernel": name, "ctas": int(ran.sum()), "sms": int(len(np.unique(sm[:n_ctas][ran]))), "stages": {}}
     for s in range(1, len(stages)):
         ok = (ns[:, s] > 0) & (ns[:, s - 1] > 0)
         if ok.any():
@@ -111,8 +112,8 @@ def run(workload: str, seed: int = 0) -> list:
         raise RuntimeError("device error word set")
     n_tiles = (w.T + 31) // 32
     rows = []
-    if n_tiles <= 32:
-        rows.append(summarize(3, n_tiles))
+    if n_tiles <= 32:  # one plan launch: a cluster of up to 16 CTAs (tiles of 8 to 32 tokens) or <= 32 CTAs
+        rows.append(summarize(3, 32))
     else:
         rows += [summarize(0, n_tiles), summarize(1, (w.P + 7) // 8), summarize(2, (w.rows + 255) // 256)]
     rows.append(summarize(4, min(TRACE_CTAS, (w.T * ((w.H + 511) // 512) + 7) // 8)))

@@ -284,11 +284,12 @@ def test_launch_count():
     _check_all(big, inp, Run(big, inp, pool=pool))
 
 
-@pytest.mark.parametrize("T", [96, 512, 1000])
+@pytest.mark.parametrize("T", [40, 96, 200, 512, 1000])
 def test_step_captures_in_a_cuda_graph(T):
     """plan -> dispatch -> combine (PDL launches) captured once in a CUDA graph
-    and replayed on new input contents gives the oracle's results: 96 and 512
-    tokens (the cluster plan, portable and 16-CTA) and 1000 (the ticket plan)."""
+    and replayed on new input contents gives the oracle's results: 40, 96, 200
+    and 512 tokens (cluster plans of 5 CTAs of 8 tokens, 6 of 16, 7 of 32 and
+    16 of 32) and 1000 (the ticket plan)."""
     w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T)
     pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
     inp0 = wl.make_inputs(w, seed=0)
@@ -451,15 +452,17 @@ def test_plan_path_switch_at_32_tiles():
 
 
 def test_plan_path_switch_at_cluster_sizes():
-    """Up to 8 tiles the cluster plan is portable, 9 to 16 tiles need the
-    non-portable cluster size, 17 tiles and more take the ticket plan: 256,
-    257, 512 and 513 tokens on one pool, one after the other, in both orders,
-    with the bench workload's replica map."""
+    """The cluster plan takes tiles of 8 tokens up to 64 tokens, 16 up to 128
+    and 32 up to 512; up to 256 tokens the cluster is portable (at most 8
+    CTAs), 257 to 512 need the non-portable size; 513 tokens and more take the
+    ticket plan.  Every switch point (1, 8, 9, 64, 65, 128, 129, 256, 257, 512,
+    513 tokens) on one pool, one after the other, in both orders, with the
+    bench workload's replica map."""
     rng = np.random.default_rng(13)
     E, P, k, H = 256, 288, 8, 256
     inp = wl.make_inputs(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 513))
     pool = moe.Pool(513, H, E, P, k, n_sets=2)
-    for T in (256, 257, 512, 513, 512, 257, 33, 32):
+    for T in (1, 8, 9, 64, 65, 128, 129, 256, 257, 512, 513, 512, 257, 256, 129, 128, 65, 64, 9, 8, 1, 33, 32):
         _custom(T, H, E, P, k, inp["logits"][:T], rep_off=inp["rep_off"], rep_ids=inp["rep_ids"],
                 seed=int(rng.integers(1 << 30)), T_max=513, pool=pool)
 
