@@ -51,6 +51,29 @@ MUTATIONS = [
     ("one slot written to the wrong copy",
      "slot[(size_t)t * k + j] = r;",
      "slot[(size_t)t * k + j] = r; if (j == 1 && t == 0) slot[0] = r;"),
+    ("amax over the first 127 elements of a group",
+     "for (int32_t i = 0; i < 128; ++i) {\n            float v = orc_bf16_to_f32(xs[i]);\n            if (!isfinite(v))",
+     "for (int32_t i = 0; i < 127; ++i) {\n            float v = orc_bf16_to_f32(xs[i]);\n            if (!isfinite(v))"),
+    ("tokens placed in descending order within a window",
+     "    for (int32_t t = 0; t < T; ++t) {\n        for (int32_t j = 0; j < k; ++j) {\n"
+     "            int32_t p = phys[(size_t)t * k + j];\n            int32_t r = cursor[p];",
+     "    for (int32_t t = T - 1; t >= 0; --t) {\n        for (int32_t j = 0; j < k; ++j) {\n"
+     "            int32_t p = phys[(size_t)t * k + j];\n            int32_t r = cursor[p];"),
+    ("gate sum accumulated in fp32",
+     "    double s = 0.0;\n    for (int32_t j = 0; j < k; ++j) {\n        ex[j] = exp(",
+     "    float s = 0.0f;\n    for (int32_t j = 0; j < k; ++j) {\n        ex[j] = exp("),
+    ("bf16 rounding by truncation",
+     "    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1u;",
+     "    (void)rest;"),
+    ("replica picked by expert id instead of token index",
+     "p = rep_ids[lo + (t % n)];",
+     "p = rep_ids[lo + (e % n)];"),
+    ("combine with uniform weights instead of the gates",
+     "acc = fmaf(gates[j], orc_bf16_to_f32(",
+     "acc = fmaf(1.0f / (float)k, orc_bf16_to_f32("),
+    ("top-k by absolute logit",
+     "    if (a->v > b->v) return -1;\n    if (a->v < b->v) return 1;",
+     "    if (fabsf(a->v) > fabsf(b->v)) return -1;\n    if (fabsf(a->v) < fabsf(b->v)) return 1;"),
 ]
 
 
