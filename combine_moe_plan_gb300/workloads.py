@@ -61,6 +61,22 @@ class Workload:
     def rows(self) -> int:
         return self.T * self.k
 
+    def describe(self) -> str:
+        """The synthetic inputs of a timed run, in words: the logits, the
+        activations, the replica map and the expert rows combine reads."""
+        logits = "N(0,1) logits" + (f" + Zipf({self.zipf_s:g}) expert bias" if self.zipf_s else "")
+        x = f"N(0,{self.x_sigma:g}) bf16 x"
+        if self.outlier_frac:
+            x += f" with {100 * self.outlier_frac:g} % of elements x{self.outlier_scale:g}"
+        parts = [logits, x]
+        if self.replicas:
+            parts.append(f"{self.replicas} hot experts with one extra replica")
+        ex = f"N(0,{self.ex_sigma:g}) bf16 expert rows"
+        if self.identity_experts:
+            ex += " (identity experts in the parity runs)"
+        parts.append(ex)
+        return "synthetic (seeded; " + "; ".join(parts) + ")"
+
     def algorithmic_bytes(self) -> dict:
         """Bytes each call must move at least once (no re-reads, no padding).
 

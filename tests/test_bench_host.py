@@ -101,3 +101,22 @@ def test_traffic_follows_the_kernel_source_closure(monkeypatch):
     assert bench._traffic("combine.cu", "combine_kernel", "t96_h7168_e256_k8") is None
     monkeypatch.setattr(bench, "source_hash", lambda f: "0" * 64)
     assert bench._traffic("combine.cu", "combine_kernel", wname) is None
+
+
+def test_bench_line_describes_each_workload_and_its_l2_footing():
+    """The data and l2 entries of the bench line follow the workload: its own
+    input distributions, and whether a step's bytes exceed L2 (no flush is
+    done, so only then are the figures DRAM figures)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from combine_moe_plan_gb300 import workloads as wl
+    d = {n: w.describe() for n, w in wl.WORKLOADS.items()}
+    assert "Zipf(1.2)" in d["t4096_h7168_e256p288_k8"] and "32 hot experts" in d["t4096_h7168_e256p288_k8"]
+    assert "Zipf" not in d["t96_h7168_e256_k8"] and "0.1 % of elements x50" in d["t96_h7168_e256_k8"]
+    assert "N(0,0.5) bf16 expert rows" in d["t16384_h2048_e64_k6"]
+    assert "identity experts" in d["t64_h256_e8_k2"]
+    l2 = 129 * 10**6
+    big = bench.l2_note(wl.WORKLOADS["t4096_h7168_e256p288_k8"].algorithmic_bytes()["total"], l2)
+    small = bench.l2_note(wl.WORKLOADS["t96_h7168_e256_k8"].algorithmic_bytes()["total"], l2)
+    assert big.startswith("inputs larger than L2") and "0.83 GB" in big
+    assert small.startswith("inputs fit in L2") and "not a DRAM one" in small
