@@ -270,7 +270,7 @@ def run_reference(a, w: wl.Workload):
         "impl": "reference", "metric": "dispatch+combine tokens/s (plan+dispatch+combine per step)",
         "value": v, "unit": "tokens/s", "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8+bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "int8+bf16", "data": w.describe(),
         "config": {"workload": w.name, "tokens_per_step": n_tok, "H": w.H, "E": w.E, "P": w.P, "k": w.k},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": n_thr, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
