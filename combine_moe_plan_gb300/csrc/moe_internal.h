@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <cuda_runtime.h>
 
 #include "moe.h"
@@ -92,6 +93,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Whether the current device launches thread-block clusters (looked up once).
 inline bool cluster_launch_supported() {
     static const bool v = [] {
+        // MOE_PLAN_NO_CLUSTER=1 takes the ticket plan instead (a device or a
+        // partition that refuses clusters takes it anyway, per launch).
+        const char* off = std::getenv("MOE_PLAN_NO_CLUSTER");
+        if (off != nullptr && off[0] == '1' && off[1] == '\0') return false;
         int dev = 0, ok = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&ok, cudaDevAttrClusterLaunch, dev) != cudaSuccess) {
