@@ -20,9 +20,11 @@ def _built():
 
 
 def _random_case(rng):
-    # batch sizes on both sides of every plan form's limit (1 tile; 8 and 16
-    # tiles for the cluster plan; 32 for the ticket plan) and beyond
-    T = int(rng.choice([1, 2, 31, 32, 33, 95, 256, 257, 512, 513, 700, 1024, 1025, 1500]))
+    # batch sizes on both sides of every plan form's limit: the cluster plan's
+    # tile sizes (8 tokens up to 64, 16 up to 128, 32 up to 512, portable up
+    # to 256), the ticket plan's 32 tiles, and beyond
+    T = int(rng.choice([1, 2, 8, 9, 31, 32, 33, 64, 65, 95, 128, 129, 200, 256, 257, 512, 513, 700, 1024, 1025,
+                        1500]))
     H = int(rng.choice([128, 256, 384, 896, 2048]))
     E = int(rng.integers(1, 300))
     k_max = 32 if rng.random() < 0.25 else 12
