@@ -45,9 +45,14 @@ MOE_TRACE_BUFFERS(tr_assign)
 namespace moe {
 namespace {
 
-// Batches of at most this many 32-token tiles are planned in one launch.
+// Batches of at most this many 32-token tiles that do not take the cluster
+// plan (clusters refused) are planned in one launch, the ticket kernel.  Its
+// single-CTA tail grows with the batch: as a graph it ties the three launches
+// at 3 tiles and loses from there (256 tokens 14.6 vs 13.0 us, 512 tokens
+// 18.8 vs 13.0 us, 1000 tokens 33 vs 16 us), so larger batches take the three
+// launches.
 #ifndef MOE_PLAN_SINGLE_MAX_TILES
-#define MOE_PLAN_SINGLE_MAX_TILES 32
+#define MOE_PLAN_SINGLE_MAX_TILES 4
 #endif
 
 // 2048 / THREADS CTAs per SM caps the kernel at 32 registers a thread (a few
@@ -312,8 +317,8 @@ __device__ void plan_tail(int32_t* __restrict__ tile_hist, int n_tiles, int T, i
 }
 
 // Single-launch plan for batches of at most MOE_PLAN_SINGLE_MAX_TILES tiles
-// (trace stages 0-5 as route_tile; the last CTA adds 6 scans done, 7 end)
-// (the decode regime): every CTA routes its tile; the CTA that finishes last
+// when the cluster plan is not available (trace stages 0-5 as route_tile;
+// the last CTA adds 6 scans done, 7 end): every CTA routes its tile; the CTA that finishes last
 // (atomic ticket, no waiting) then runs the column scans, the offsets and the
 // slot assignment for the whole batch, and resets the ticket for the next
 // call.  Each CTA fences its writes before taking its ticket, and the last

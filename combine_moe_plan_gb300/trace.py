@@ -112,9 +112,10 @@ def run(workload: str, seed: int = 0) -> list:
         raise RuntimeError("device error word set")
     n_tiles = (w.T + 31) // 32
     rows = []
-    if n_tiles <= 32:  # one plan launch: a cluster of up to 16 CTAs (tiles of 8 to 32 tokens) or <= 32 CTAs
-        rows.append(summarize(3, 32))
-    else:
+    one = summarize(3, 32)  # one plan launch: the cluster kernel, or the ticket kernel without clusters
+    if one["ctas"] > 0:
+        rows.append(one)
+    else:  # the three launches
         rows += [summarize(0, n_tiles), summarize(1, (w.P + 7) // 8), summarize(2, (w.rows + 255) // 256)]
     rows.append(summarize(4, min(TRACE_CTAS, (w.T * ((w.H + 511) // 512) + 7) // 8)))
     rows.append(summarize(5, min(TRACE_CTAS, (w.T * ((w.H + 255) // 256) + 7) // 8)))

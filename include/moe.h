@@ -183,11 +183,12 @@ MOE_API int moe_replica_check(const int32_t* rep_off, const int32_t* rep_ids, in
  * src_token / src_k.  Writes topk_e, gates, phys, counts, offsets, slot,
  * src_token, src_k of the set.  0 <= T <= T_max; T = 0 (an empty batch)
  * zeroes counts and offsets and launches no kernel (logits may be NULL).
- * Kernels: up to 512 tokens one thread-block cluster; up to 1024 one
- * launch whose last CTA finishes the placement; beyond, three launches.
- * With the environment variable MOE_PLAN_NO_CLUSTER=1 (read once per
- * process), or on a device that refuses the cluster, batches of up to 512
- * tokens take the one-launch form too.  The results do not depend on the form.
+ * Kernels: up to 512 tokens one thread-block cluster; beyond, three
+ * launches (route, column scan, assign).  With the environment variable
+ * MOE_PLAN_NO_CLUSTER=1 (read once per process), or on a device that refuses
+ * the cluster, batches of up to 128 tokens take one launch whose last CTA
+ * finishes the placement, and larger ones the three launches.  The results
+ * do not depend on the form.
  */
 MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T,
                      const int32_t* rep_off, const int32_t* rep_ids, int buf, void* stream);

@@ -22,7 +22,7 @@ def _built():
 def _random_case(rng):
     # batch sizes on both sides of every plan form's limit: the cluster plan's
     # tile sizes (8 tokens up to 64, 16 up to 128, 32 up to 512, portable up
-    # to 256), the ticket plan's 32 tiles, and beyond
+    # to 256), the three launches beyond, and 32/33 tiles
     T = int(rng.choice([1, 2, 8, 9, 31, 32, 33, 64, 65, 95, 128, 129, 200, 256, 257, 512, 513, 700, 1024, 1025,
                         1500]))
     H = int(rng.choice([128, 256, 384, 896, 2048]))

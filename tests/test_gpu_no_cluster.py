@@ -1,9 +1,10 @@
 """The plan without thread-block clusters.  A device or partition that refuses
-the cluster launch plans batches of up to 512 tokens with the one-launch
-ticket kernel instead; MOE_PLAN_NO_CLUSTER=1 forces that path.  The cluster
-plan's parity tests (every switch point from 1 to 513 tokens, graph capture,
-chained layers, fuzz over small batches) are re-run in a child process with
-the variable set, so the same oracle comparisons cover the fallback."""
+the cluster launch plans batches of up to 128 tokens with the one-launch
+ticket kernel instead, and larger ones with the three launches;
+MOE_PLAN_NO_CLUSTER=1 forces that.  The cluster plan's parity tests (every
+switch point from 1 to 513 tokens, graph capture, chained layers, the small
+workloads) are re-run in a child process with the variable set, so the same
+oracle comparisons cover the fallback."""
 import os
 import subprocess
 import sys

@@ -289,7 +289,7 @@ def test_step_captures_in_a_cuda_graph(T):
     """plan -> dispatch -> combine (PDL launches) captured once in a CUDA graph
     and replayed on new input contents gives the oracle's results: 40, 96, 200
     and 512 tokens (cluster plans of 5 CTAs of 8 tokens, 6 of 16, 7 of 32 and
-    16 of 32) and 1000 (the ticket plan)."""
+    16 of 32) and 1000 (the three launches)."""
     w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T)
     pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
     inp0 = wl.make_inputs(w, seed=0)
@@ -438,9 +438,9 @@ def test_step_host_matches_oracle():
     assert pool.check() == 0
 
 
-def test_plan_path_switch_at_32_tiles():
-    """1024 tokens (32 tiles) take the single-launch plan, 1025 (33 tiles) the
-    three launches; both on one pool, one after the other, in both orders."""
+def test_plan_at_32_and_33_tiles():
+    """1024 tokens (32 tiles) and 1025 (33 tiles, a ragged tail of one token)
+    through the three launches on one pool, one after the other."""
     rng = np.random.default_rng(12)
     E, P, k, H = 256, 288, 8, 256
     w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
@@ -455,7 +455,7 @@ def test_plan_path_switch_at_cluster_sizes():
     """The cluster plan takes tiles of 8 tokens up to 64 tokens, 16 up to 128
     and 32 up to 512; up to 256 tokens the cluster is portable (at most 8
     CTAs), 257 to 512 need the non-portable size; 513 tokens and more take the
-    ticket plan.  Every switch point (1, 8, 9, 64, 65, 128, 129, 256, 257, 512,
+    three launches (and without clusters, 129 tokens and more).  Every switch point (1, 8, 9, 64, 65, 128, 129, 256, 257, 512,
     513 tokens) on one pool, one after the other, in both orders, with the
     bench workload's replica map."""
     rng = np.random.default_rng(13)
