@@ -48,7 +48,7 @@ namespace {
 // Batches of at most this many 32-token tiles that do not take the cluster
 // plan (clusters refused) are planned in one launch, the ticket kernel.  Its
 // single-CTA tail grows with the batch: as a graph it ties the three launches
-// at 3 tiles and loses from there (256 tokens 14.6 vs 13.0 us, 512 tokens
+// at 3 tiles and loses at 8 and more (256 tokens 14.6 vs 13.0 us, 512 tokens
 // 18.8 vs 13.0 us, 1000 tokens 33 vs 16 us), so larger batches take the three
 // launches.
 #ifndef MOE_PLAN_SINGLE_MAX_TILES
