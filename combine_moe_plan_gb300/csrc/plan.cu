@@ -628,7 +628,7 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
     // is not stretched by waiting for SM slots.
     const int urgent = most_urgent_priority();
     cudaError_t e;
-    if (ticket != nullptr && n_tiles <= kClusterTiles && cluster_launch_supported()) {
+    if (n_tiles <= kClusterTiles && cluster_launch_supported()) {  // needs no ticket and no scratch
         // The smallest tile that keeps the cluster portable (at most 8 CTAs);
         // 32-token tiles beyond that, in up to kClusterTiles CTAs.
         const int epl = (E + 31) / 32;

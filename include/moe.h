@@ -261,7 +261,10 @@ MOE_API int moe_step_host(moe_pool* pool, const float* h_logits, const uint16_t*
  * MOE_ERR_SIZE before anything is launched.  No cudaMalloc or cudaFree is
  * called.
  *   - All calls share that array: calls whose kernels overlap on the GPU
- *     (other streams, other host threads) race and give wrong slots.
+ *     (other streams, other host threads) race and give wrong slots.  Batches
+ *     of up to 512 tokens take the cluster plan, which keeps its scratch in
+ *     shared memory and does not touch the array, where the device launches
+ *     clusters (not with MOE_PLAN_NO_CLUSTER=1).
  *   - The first call on each device looks up the array's device address with
  *     that device current; make it before any stream capture begins.
  */

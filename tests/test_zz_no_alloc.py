@@ -43,7 +43,8 @@ def _compare(got, ref, what):
 
 def test_plan_static_matches_plan_two_calls_in_a_row():
     ensure_built()
-    cases = [wl.WORKLOADS["t4096_h7168_e256p288_k8"], wl.small_variant(wl.WORKLOADS["t16384_h2048_e64_k6"], 3000)]
+    cases = [wl.WORKLOADS["t4096_h7168_e256p288_k8"], wl.small_variant(wl.WORKLOADS["t16384_h2048_e64_k6"], 3000),
+             wl.WORKLOADS["t96_h7168_e256_k8"]]
     refs, gots = [], []
     for w in cases:
         inp = wl.make_inputs(w, with_expert_out=False)
@@ -55,6 +56,34 @@ def test_plan_static_matches_plan_two_calls_in_a_row():
     torch.cuda.synchronize()
     for w, got, ref in zip(cases, gots, refs):
         _compare(got, ref, w.name)
+
+
+def test_plan_static_small_batches_overlap_on_two_streams():
+    """Batches of up to 512 tokens take the cluster plan, which keeps its
+    scratch in shared memory: calls on two streams may overlap on the GPU and
+    still give moe_plan's results (96 and 300 tokens, 20 rounds, no
+    synchronization between the streams)."""
+    ensure_built()
+    ws = [wl.WORKLOADS["t96_h7168_e256_k8"], wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 300)]
+    args, refs = [], []
+    for w in ws:
+        inp = wl.make_inputs(w, with_expert_out=False)
+        logits = dev(inp["logits"])
+        ro = None if inp["rep_off"] is None else dev(inp["rep_off"])
+        ri = None if inp["rep_ids"] is None else dev(inp["rep_ids"])
+        args.append((w, logits, ro, ri))
+        refs.append(_pool_plan(w, logits, ro, ri))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[], []]
+    torch.cuda.synchronize()
+    for _ in range(20):
+        for i, (w, logits, ro, ri) in enumerate(args):
+            with torch.cuda.stream(streams[i]):
+                outs[i].append(moe.plan_static(logits, w.k, w.P, ro, ri, stream=streams[i]))
+    torch.cuda.synchronize()
+    for i, (w, _, _, _) in enumerate(args):
+        for r, got in enumerate(outs[i]):
+            _compare(got, refs[i], f"{w.name} round {r}")
 
 
 def test_plan_static_rejects_oversized_scratch():
