@@ -478,6 +478,19 @@ def test_three_launch_plan_at_maximum_shapes():
     _custom(1100, 128, E, P, 32, rng.standard_normal((1100, E)), rep_off=off, rep_ids=ids)
 
 
+@pytest.mark.parametrize("T", [60, 100, 300])
+def test_cluster_plan_at_maximum_shapes(T):
+    """The cluster plan at the largest shapes the API takes (E = 1024, P =
+    4096 with four replicas per expert, k = 32), for each tile size: 60 tokens
+    (8 CTAs of 8), 100 (7 of 16), 300 (10 of 32, non-portable) -- its largest
+    shared-memory footprint (about 85 KB a CTA) and 32 keys a lane."""
+    rng = np.random.default_rng(20 + T)
+    E, P = 1024, 4096
+    off = np.arange(0, P + 1, 4, dtype=np.int32)
+    ids = rng.permutation(P).astype(np.int32)
+    _custom(T, 128, E, P, 32, rng.standard_normal((T, E)), rep_off=off, rep_ids=ids, seed=T)
+
+
 def test_bench_schedule_two_streams_full_size():
     """The bench's timed schedule at the bench workload's full size: steps
     alternate the two buffer sets on two streams, launched back to back, each
