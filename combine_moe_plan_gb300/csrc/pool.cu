@@ -99,6 +99,15 @@ int check_call(const moe_pool* pool, int32_t T, int buf) {
     return MOE_OK;
 }
 
+// The replica-map arguments of a non-empty plan: both pointers or neither
+// (neither requires P == E), each 16-byte aligned.
+int check_replica_args(const moe_desc& d, const int32_t* rep_off, const int32_t* rep_ids) {
+    if ((rep_off == nullptr) != (rep_ids == nullptr)) return MOE_ERR_NULL;
+    if (rep_off == nullptr && d.P != d.E) return MOE_ERR_REPLICA;
+    if (rep_off != nullptr && (!aligned16(rep_off) || !aligned16(rep_ids))) return MOE_ERR_ALIGN;
+    return MOE_OK;
+}
+
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 }  // namespace
@@ -214,9 +223,7 @@ MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T, const int32
     }
     if (logits == nullptr) return MOE_ERR_NULL;
     if (!aligned16(logits)) return MOE_ERR_ALIGN;
-    if ((rep_off == nullptr) != (rep_ids == nullptr)) return MOE_ERR_NULL;
-    if (rep_off == nullptr && d.P != d.E) return MOE_ERR_REPLICA;
-    if (rep_off != nullptr && (!aligned16(rep_off) || !aligned16(rep_ids))) return MOE_ERR_ALIGN;
+    if ((rc = check_replica_args(d, rep_off, rep_ids)) != MOE_OK) return rc;
     cudaError_t e = launch_plan(logits, T, d.E, d.P, d.k, rep_off, rep_ids, at<int32_t>(pool, L.topk_e),
                                 at<float>(pool, L.gates), at<int32_t>(pool, L.phys),
                                 at<int32_t>(pool, L.tile_hist), at<int32_t>(pool, L.local_rank),
@@ -280,6 +287,9 @@ MOE_API int moe_step_host(moe_pool* pool, const float* h_logits, const uint16_t*
     if (T == 0) return moe_plan(pool, h_logits, 0, rep_off, rep_ids, buf, stream);
     if (h_logits == nullptr || h_x == nullptr || h_y == nullptr) return MOE_ERR_NULL;
     const moe_desc& d = pool->geo.d;
+    // Everything moe_plan would reject is rejected before the first copy, so
+    // that on an error nothing is enqueued.
+    if ((rc = check_replica_args(d, rep_off, rep_ids)) != MOE_OK) return rc;
     const SetLayout& L = pool->geo.set[buf];
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* logits = at<float>(pool, L.logits_stage);

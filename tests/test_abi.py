@@ -131,6 +131,25 @@ def test_replica_map_needed_when_P_exceeds_E(L):
     L.moe_pool_destroy(h)
 
 
+def test_step_host_rejects_before_enqueueing(L):
+    """moe_step_host checks everything moe_plan would reject before its first
+    copy: with no GPU here, a check that ran after a copy could only report
+    MOE_ERR_CUDA (-6), so these codes show that nothing was enqueued."""
+    h, _ = _fake_pool(L, E=8, P=10)
+    host = ctypes.c_void_p(1 << 41)
+    odd = ctypes.c_void_p((1 << 41) + 4)
+    step = L.moe_step_host
+    assert step(None, host, host, None, host, 8, None, None, 0, None) == -1
+    assert step(h, host, host, None, host, 8, None, None, 2, None) == -4     # bad set
+    assert step(h, host, host, None, host, 65, None, None, 0, None) == -2    # T > T_max
+    assert step(h, None, host, None, host, 8, None, None, 0, None) == -1     # no logits
+    assert step(h, host, host, None, None, 8, None, None, 0, None) == -1     # no y
+    assert step(h, host, host, None, host, 8, host, None, 0, None) == -1     # half a replica map
+    assert step(h, host, host, None, host, 8, None, None, 0, None) == -8     # P > E needs a map
+    assert step(h, host, host, None, host, 8, odd, host, 0, None) == -3      # misaligned map
+    L.moe_pool_destroy(h)
+
+
 def test_replica_check(L):
     def rc(off, ids, E, P):
         return moe.replica_check(np.array(off), np.array(ids), E, P)
