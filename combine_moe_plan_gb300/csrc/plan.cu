@@ -647,7 +647,8 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
         }
         // A cluster this size that cannot be placed is a launch-time error
         // (nothing was enqueued and the context stays usable): clear it and
-        // use the ticket kernel instead.
+        // use the ticket kernel (up to MOE_PLAN_SINGLE_MAX_TILES tiles) or
+        // the three launches instead.
         (void)cudaGetLastError();
     }
     if (ticket != nullptr && n_tiles <= MOE_PLAN_SINGLE_MAX_TILES) {
