@@ -71,6 +71,9 @@ MUTATIONS = [
     ("combine with uniform weights instead of the gates",
      "acc = fmaf(gates[j], orc_bf16_to_f32(",
      "acc = fmaf(1.0f / (float)k, orc_bf16_to_f32("),
+    ("identity experts with the next group's scale",
+     "scales[(size_t)r * G + i / 128]",
+     "scales[(size_t)r * G + (i / 128 + 1) % G]"),
     ("top-k by absolute logit",
      "    if (a->v > b->v) return -1;\n    if (a->v < b->v) return 1;",
      "    if (fabsf(a->v) > fabsf(b->v)) return -1;\n    if (fabsf(a->v) < fabsf(b->v)) return 1;"),
