@@ -272,7 +272,7 @@ def test_launch_count():
     pool = moe.Pool(64, w.H, w.E, w.P, w.k)
     n0 = pool.launches()
     Run(w, inp, pool=pool)
-    # a 64-token plan is one launch (two tiles); then dispatch, identity experts, combine
+    # a 64-token plan is one launch (the cluster plan); then dispatch, identity experts, combine
     assert pool.launches() - n0 == 4
     # a 1056-token plan (33 tiles) takes the three-launch path
     big = wl.small_variant(wl.WORKLOADS["t64_h256_e8_k2"], 1056)
@@ -455,9 +455,10 @@ def test_plan_path_switch_at_cluster_sizes():
     """The cluster plan takes tiles of 8 tokens up to 64 tokens, 16 up to 128
     and 32 up to 512; up to 256 tokens the cluster is portable (at most 8
     CTAs), 257 to 512 need the non-portable size; 513 tokens and more take the
-    three launches (and without clusters, 129 tokens and more).  Every switch point (1, 8, 9, 64, 65, 128, 129, 256, 257, 512,
-    513 tokens) on one pool, one after the other, in both orders, with the
-    bench workload's replica map."""
+    three launches (and without clusters, 129 tokens and more).  Every switch
+    point (1, 8, 9, 64, 65, 128, 129, 256, 257, 512, 513 tokens) on one pool,
+    one after the other, in both orders, with the bench workload's replica
+    map."""
     rng = np.random.default_rng(13)
     E, P, k, H = 256, 288, 8, 256
     inp = wl.make_inputs(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 513))
@@ -539,8 +540,9 @@ def test_layers_chained_on_one_stream(name, T):
     equals the oracle run layer after layer on its own outputs.  Dispatch reads
     x before its wait for the plan, so this checks that the previous layer's
     combine has finished writing x by then (the plan in between waits for it).
-    The plan forms covered: cluster (96, 300 tokens), one launch (1000), three
-    launches (2000)."""
+    The plan forms covered: cluster (96 tokens as 6 CTAs of 16, 300 as 10 of
+    32) and three launches (1000 and 2000 tokens, 8-lane segments at 64
+    experts); the test run without clusters adds the ticket kernel."""
     w = wl.small_variant(wl.WORKLOADS[name], T)
     L = 6
     layers = [wl.make_inputs(w, seed=10 + l, with_expert_out=False) for l in range(L)]
