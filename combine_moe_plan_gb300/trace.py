@@ -29,8 +29,10 @@ KINDS = {
     0: ("route_tile", ["start", "top-k", "gates(pairs)", "fallback", "replicas+masks", "counts+ranks"]),
     1: ("column_scan", ["start", "end"]),
     2: ("assign", ["start", "offsets", "end"]),
-    3: ("plan_single", ["start", "top-k", "gates(pairs)", "fallback", "replicas+masks", "counts+ranks",
-                        "handoff", "end"]),
+    # one plan launch: the cluster kernel (stage 6 = cluster barrier passed) or,
+    # without clusters, the ticket kernel (stage 6 = its last CTA's scans done)
+    3: ("plan_one_launch", ["start", "top-k", "gates(pairs)", "fallback", "replicas+masks", "counts+ranks",
+                            "barrier|scans", "end"]),
     4: ("dispatch", ["start", "quantized", "slots", "stored"]),
     5: ("combine", ["start", "slots", "accumulated", "stored"]),
 }

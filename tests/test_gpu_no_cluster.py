@@ -37,7 +37,7 @@ def _plan_ctas(env) -> int:
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     rows = [json.loads(line) for line in r.stdout.splitlines() if line.startswith("{")]
-    return next(x["ctas"] for x in rows if x["kernel"] == "plan_single")
+    return next(x["ctas"] for x in rows if x["kernel"] == "plan_one_launch")
 
 
 def test_the_switch_selects_the_ticket_plan():

@@ -20,7 +20,7 @@ def test_trace_stages(workload):
     rows = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
     names = [x["kernel"] for x in rows]
     if workload.startswith("t96"):
-        assert names == ["plan_single", "dispatch", "combine"]
+        assert names == ["plan_one_launch", "dispatch", "combine"]
     else:
         assert names == ["route_tile", "column_scan", "assign", "dispatch", "combine"]
     for x in rows:
@@ -29,4 +29,4 @@ def test_trace_stages(workload):
             assert st["median_ns"] >= 0 and st["ctas"] >= 1
         # every CTA of the launch was stamped at its first and last stage
         first = next(iter(x["stages"].values()))
-        assert first["ctas"] == x["ctas"] or x["kernel"] in ("plan_single",)
+        assert first["ctas"] == x["ctas"] or x["kernel"] in ("plan_one_launch",)
