@@ -154,17 +154,25 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 9]
-        if not rows:
-            return None
-        sm = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.strip() == "Active"})
-        # samples under load: SM clock above the idle floor
-        load = [s for s in sm if s > 0.5 * (max(sm) if sm else 1)]
-        return {"sm_mhz": statistics.median(load) if load else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+        return parse_clocks(out)
+
+
+def parse_clocks(out: str):
+    """Summary of nvidia-smi samples in ClockSampler.Q's column order
+    (csv, noheader, nounits): the median SM clock under load (samples above
+    half the largest), the largest max clock, every throttle reason seen
+    Active, and the sample count; None without samples."""
+    rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 9]
+    if not rows:
+        return None
+    sm = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+    mx = [float(r[3]) for r in rows if r[3].strip().replace(".", "").isdigit()]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.strip() == "Active"})
+    # samples under load: SM clock above the idle floor
+    load = [s for s in sm if s > 0.5 * (max(sm) if sm else 1)]
+    return {"sm_mhz": statistics.median(load) if load else None,
+            "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
 def _dist():

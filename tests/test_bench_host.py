@@ -120,3 +120,21 @@ def test_bench_line_describes_each_workload_and_its_l2_footing():
     small = bench.l2_note(wl.WORKLOADS["t96_h7168_e256_k8"].algorithmic_bytes()["total"], l2)
     assert big.startswith("inputs larger than L2") and "0.83 GB" in big
     assert small.startswith("inputs fit in L2") and "not a DRAM one" in small
+
+
+def test_clock_samples_are_summarised_and_throttling_is_seen():
+    """The clocks entry of the bench line: median SM clock under load, the
+    maximum, and every throttle reason sampled Active (a run that saw a
+    hardware or thermal slowdown is not a valid measurement)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    def row(sm, reasons=("Not Active",) * 4):
+        return ", ".join(["2026/12/02 12:00:00.000", "0", str(sm), "2070", "900.1", "0x0"] + list(reasons))
+    idle = [row(345)] * 3
+    load = [row(2070)] * 7 + [row(2055)]
+    c = bench.parse_clocks("\n".join(idle + load + ["garbled line"]))
+    assert c == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 11}
+    hot = row(1800, ("Active", "Not Active", "Not Active", "Active"))
+    c = bench.parse_clocks("\n".join(load + [hot]))
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert bench.parse_clocks("") is None
