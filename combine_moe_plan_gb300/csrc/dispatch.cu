@@ -26,6 +26,10 @@ namespace {
 
 constexpr int kDispatchThreads = 256;  // 8 warps, 8 (token, segment) items per CTA
 
+// X_EARLY: load and quantize x before waiting for the preceding kernel
+// (moe_dispatch_after_plan); otherwise x is read after the wait, like every
+// other input (moe_dispatch).
+template <bool X_EARLY>
 __global__ void __launch_bounds__(kDispatchThreads)
 dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ slot,
                 int8_t* __restrict__ codes, float* __restrict__ scales, int Gs, int32_t* __restrict__ err) {
@@ -40,20 +44,21 @@ dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, const int32
     const int seg = (int)(item - (long long)t * segs);
     if (t >= T) return;
 
-    // x is loaded and quantized before the wait for the previous kernel.  That
-    // kernel is the plan, which does not write x and lets its dependents start
-    // only after its own wait has returned, i.e. once everything before it on
-    // the stream has completed and its writes are visible; so x is final here.
-    // include/moe.h makes this a precondition of moe_dispatch (the kernel
-    // launched just before it must not write x and must let its dependents
-    // start only after its own wait).  The slots come from the
-    // plan: read after the wait.  Dependents may start only after the wait, as
-    // in every kernel of the library, so that whatever runs next on the stream
-    // sees all writes made before this kernel.
+    // In the X_EARLY form x is loaded and quantized before the wait.  That is
+    // correct only when the kernel launched just before this one never writes
+    // x and lets its dependents start only after its own wait has returned
+    // (then everything earlier on the stream has completed and its writes are
+    // visible): the plan kernels meet both, and moe_dispatch_after_plan makes
+    // this the caller's precondition.  The default form waits first.  The
+    // slots come from the plan and are always read after the wait.
+    // Dependents may start only after the wait, as in every kernel of the
+    // library, so that whatever runs next on the stream sees all writes made
+    // before this kernel.
+    if (!X_EARLY) grid_dependency_sync();
     const SegLoad ld = load_segment(x, t, H, seg, lane);
     const SegQuant qz = quantize_segment(ld);
     MOE_TRACE_MARK(tr_dispatch, 1);
-    grid_dependency_sync();
+    if (X_EARLY) grid_dependency_sync();
     allow_dependents();
     const int my_slot = (lane < k) ? slot[(size_t)t * k + lane] : 0;
     MOE_TRACE_MARK(tr_dispatch, 2);
@@ -104,11 +109,13 @@ int trace_symbols_dispatch(void** stamps, void** sms) {
 #endif
 
 cudaError_t launch_dispatch(const uint16_t* x, int T, int H, int k, const int32_t* slot, int8_t* codes,
-                            float* scales, int Gs, int32_t* err, cudaStream_t s, uint64_t* launches) {
+                            float* scales, int Gs, int32_t* err, bool x_early, cudaStream_t s, uint64_t* launches) {
     const long long items = (long long)T * ((H + kSegElems - 1) / kSegElems);
     const long long blocks = (items + (kDispatchThreads / 32) - 1) / (kDispatchThreads / 32);
-    cudaError_t e = launch_pdl(dispatch_kernel, dim3((unsigned)blocks), dim3(kDispatchThreads), 0, s, x, T, H, k,
-                               slot, codes, scales, Gs, err);
+    cudaError_t e = x_early ? launch_pdl(dispatch_kernel<true>, dim3((unsigned)blocks), dim3(kDispatchThreads), 0, s,
+                                         x, T, H, k, slot, codes, scales, Gs, err)
+                            : launch_pdl(dispatch_kernel<false>, dim3((unsigned)blocks), dim3(kDispatchThreads), 0,
+                                         s, x, T, H, k, slot, codes, scales, Gs, err);
     if (e == cudaSuccess) *launches += 1;
     return e;
 }

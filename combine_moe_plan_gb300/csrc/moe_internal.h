@@ -133,8 +133,9 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k,
                         int32_t* ticket /* zeroed int32, or NULL: always three launches */,
                         cudaStream_t s, uint64_t* launches);
 
+// x_early: read x before waiting for the preceding kernel (see moe_dispatch_after_plan).
 cudaError_t launch_dispatch(const uint16_t* x, int T, int H, int k, const int32_t* slot,
-                            int8_t* codes, float* scales, int Gs, int32_t* err,
+                            int8_t* codes, float* scales, int Gs, int32_t* err, bool x_early,
                             cudaStream_t s, uint64_t* launches);
 
 cudaError_t launch_identity_experts(const int8_t* codes, const float* scales, int rows, int H, int Gs,

@@ -237,7 +237,11 @@ MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T, const int32
     return MOE_OK;
 }
 
-MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int dispatch_call(moe_pool* pool, const uint16_t* x, int32_t T, int buf, bool x_early, void* stream) {
     int rc = check_call(pool, T, buf);
     if (rc != MOE_OK) return rc;
     if (T > 0 && x == nullptr) return MOE_ERR_NULL;
@@ -248,8 +252,20 @@ MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, 
     const SetLayout& L = pool->geo.set[buf];
     return cuda_rc(launch_dispatch(x, T, d.H, d.k, at<int32_t>(pool, L.slot), at<int8_t>(pool, L.codes),
                                    at<float>(pool, L.scales), pool->geo.Gs,
-                                   at<int32_t>(pool, pool->geo.error_word), static_cast<cudaStream_t>(stream),
-                                   &pool->launches));
+                                   at<int32_t>(pool, pool->geo.error_word), x_early,
+                                   static_cast<cudaStream_t>(stream), &pool->launches));
+}
+
+}  // namespace
+
+extern "C" {
+
+MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream) {
+    return dispatch_call(pool, x, T, buf, false, stream);
+}
+
+MOE_API int moe_dispatch_after_plan(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream) {
+    return dispatch_call(pool, x, T, buf, true, stream);
 }
 
 MOE_API int moe_identity_experts(moe_pool* pool, int32_t T, int buf, void* stream) {
@@ -301,7 +317,8 @@ MOE_API int moe_step_host(moe_pool* pool, const float* h_logits, const uint16_t*
         cudaMemcpyAsync(x, h_x, TH * sizeof(uint16_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if ((rc = moe_plan(pool, logits, T, rep_off, rep_ids, buf, stream)) != MOE_OK) return rc;
-    if ((rc = moe_dispatch(pool, x, T, buf, stream)) != MOE_OK) return rc;
+    // The plan is the kernel just before, and x came in by a copy before it.
+    if ((rc = moe_dispatch_after_plan(pool, x, T, buf, stream)) != MOE_OK) return rc;
     if (h_ex_out != nullptr) {
         if (cudaMemcpyAsync(at<uint16_t>(pool, L.ex_out), h_ex_out, (size_t)T * d.k * d.H * sizeof(uint16_t),
                             cudaMemcpyHostToDevice, s) != cudaSuccess)

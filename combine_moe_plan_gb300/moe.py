@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
         "moe_replica_check": [vp, vp, i32, i32],
         "moe_plan": [vp, vp, i32, vp, vp, ctypes.c_int, vp],
         "moe_dispatch": [vp, vp, i32, ctypes.c_int, vp],
+        "moe_dispatch_after_plan": [vp, vp, i32, ctypes.c_int, vp],
         "moe_identity_experts": [vp, i32, ctypes.c_int, vp],
         "moe_combine": [vp, vp, vp, i32, ctypes.c_int, vp],
         "moe_step_host": [vp, vp, vp, vp, vp, i32, vp, vp, ctypes.c_int, vp],
@@ -189,8 +190,12 @@ class Pool:
         _call("moe_plan", self.handle, _ptr(logits), T, _ptr(rep_off), _ptr(rep_ids), buf, _stream(stream))
         return T
 
-    def dispatch(self, x, buf=0, stream=None):
-        _call("moe_dispatch", self.handle, _ptr(x), x.shape[0], buf, _stream(stream))
+    def dispatch(self, x, buf=0, stream=None, after_plan=False):
+        """moe_dispatch; with ``after_plan`` moe_dispatch_after_plan, which
+        reads x before waiting for the kernel just before it: only right after
+        this set's plan on the same stream, with x written before that plan."""
+        fn = "moe_dispatch_after_plan" if after_plan else "moe_dispatch"
+        _call(fn, self.handle, _ptr(x), x.shape[0], buf, _stream(stream))
 
     def identity_experts(self, T, buf=0, stream=None):
         _call("moe_identity_experts", self.handle, T, buf, _stream(stream))

@@ -36,15 +36,11 @@
  *     moe_pool_check and moe_step_host's documented copies.
  *   - Kernels are launched with programmatic dependent launch: each may start
  *     while the kernel before it on the stream drains, and waits for it
- *     (griddepcontrol.wait) before reading what it may have written; each
- *     lets its own dependents start only after that wait.  The one exception
- *     is moe_dispatch, which reads x before its wait.  So the kernel launched
- *     immediately before moe_dispatch on `stream` must not write x, and if
- *     that kernel was itself launched with programmatic dependent launch it
- *     must let its dependents start only after its own wait.  Every kernel of
- *     this library meets the second condition; moe_plan, the usual
- *     predecessor, also never writes x.  Writes by anything earlier in stream
- *     order, or by a memory copy right before moe_dispatch, are seen.
+ *     (griddepcontrol.wait) before reading any input; each lets its own
+ *     dependents start only after that wait.  So every input written earlier
+ *     in stream order, by any kernel or copy, is seen.  The one opt-in
+ *     exception is moe_dispatch_after_plan, which reads x before its wait
+ *     (see there).
  *   - The caller owns every buffer, including the pool workspace; the library
  *     never allocates device memory.
  *   - Inputs outside the documented domain (non-finite logits or activations,
@@ -127,38 +123,59 @@ typedef struct moe_view {
     int32_t scale_stride;/* Gs */
 } moe_view;
 
-/* Bytes of device workspace a pool with this geometry needs.  Host only. */
+/*
+ * The pool calls below serve the statically pre-allocated, double-buffered
+ * per-expert buffers (write-up, "FusedDispatch and FusedCombine":
+ * "Double-Buffered Static Pre-allocation"): buffers sized once for the worst
+ * case, carved from one workspace, reused by every layer call.
+ */
+
+/*
+ * Bytes of device workspace a pool with this geometry needs: every set's
+ * dispatch and combine buffers at worst-case capacity ("Double-Buffered
+ * Static Pre-allocation").  Host only.
+ */
 MOE_API int moe_pool_bytes(const moe_desc* desc, size_t* bytes);
 
 /*
  * Create a pool over a caller-owned device workspace of at least
- * moe_pool_bytes(desc) bytes, 256-byte aligned.  Host only: nothing is
- * launched and the workspace is not touched; call moe_pool_clear_error once
- * before first use.  The workspace must outlive the pool.
+ * moe_pool_bytes(desc) bytes, 256-byte aligned.  The buffers are carved here
+ * once and never allocated again ("Double-Buffered Static Pre-allocation").
+ * Host only: nothing is launched and the workspace is not touched; call
+ * moe_pool_clear_error once before first use.  The workspace must outlive
+ * the pool.
  */
 MOE_API int moe_pool_init(const moe_desc* desc, void* dev_ws, size_t ws_bytes, moe_pool** out);
 
-/* Free the host handle (the workspace stays the caller's). */
+/* Free the host handle; the workspace, and with it the pre-allocated buffers
+ * ("Double-Buffered Static Pre-allocation"), stay the caller's. */
 MOE_API int moe_pool_destroy(moe_pool* pool);
 
-/* Device addresses of buffer set `buf`. */
+/* Device addresses of buffer set `buf`: its pre-allocated dispatch and
+ * combine buffers and plan metadata ("Double-Buffered Static
+ * Pre-allocation": one of the double-buffered sets). */
 MOE_API int moe_pool_view(const moe_pool* pool, int buf, moe_view* view);
 
 /*
- * Zero the device error word and the pool's plan tickets (asynchronous on
- * `stream`).  Call once before the pool's first use, after any
- * MOE_ERR_DEVICE, and never while the pool's kernels run on another stream.
+ * Zero the device error word and the pool's plan tickets, the control block
+ * in front of the pre-allocated sets ("Double-Buffered Static
+ * Pre-allocation"), asynchronously on `stream`.  Call once before the pool's
+ * first use, after any MOE_ERR_DEVICE, and never while the pool's kernels
+ * run on another stream.
  */
 MOE_API int moe_pool_clear_error(moe_pool* pool, void* stream);
 
 /*
  * Synchronize `stream`, read the device error word into *error_word (may be
- * NULL) and return MOE_ERR_DEVICE if any bit is set, else MOE_OK.  The word
+ * NULL) and return MOE_ERR_DEVICE if any bit is set, else MOE_OK.  The bits
+ * record bad indices the kernels skipped instead of writing outside the
+ * pre-allocated buffers ("Double-Buffered Static Pre-allocation").  The word
  * is not cleared.
  */
 MOE_API int moe_pool_check(moe_pool* pool, void* stream, int32_t* error_word);
 
-/* Number of kernels this pool has launched since init. */
+/* Number of kernels launched on this pre-allocated pool since init
+ * ("Double-Buffered Static Pre-allocation"). */
 MOE_API int moe_pool_launches(const moe_pool* pool, uint64_t* count);
 
 /*
@@ -194,17 +211,31 @@ MOE_API int moe_plan(moe_pool* pool, const float* logits, int32_t T,
                      const int32_t* rep_off, const int32_t* rep_ids, int buf, void* stream);
 
 /*
- * moe_dispatch: quantize x and scatter into the set's dispatch rows.
+ * moe_dispatch: quantize x and scatter into the set's dispatch rows
+ * (write-up, "FusedDispatch and FusedCombine": "Early INT8 Quantization",
+ * "AIV-Direct Write", "Token-Level Pipeline").
  *   x  device bf16 [T, H]
  * Per token and 128-element group g: amax = max |x|, scale = amax / 127 (fp32),
  * code = rint((x * 127) / amax) in fp32, half-even (amax = 0: scale 0, codes 0).
  * Row slot[t, j] of codes / scales receives token t's codes / scales for every
  * j.  Requires a prior moe_plan on this set with the same T (T = 0: no-op).
- * x is read before the wait for the preceding kernel: the kernel launched
- * just before this call on `stream` must not write x and must not let its
- * dependents start before its own wait (see the conventions).
+ * x may be written by anything earlier on `stream`, kernels included.
  */
 MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream);
+
+/*
+ * moe_dispatch_after_plan: moe_dispatch for the plan -> dispatch sequence,
+ * with x loaded and quantized while the plan still runs (same passages, same
+ * results, about half a microsecond earlier on a 96-token batch).  x is read
+ * BEFORE the wait for the preceding kernel, so this is correct only when the
+ * kernel enqueued just before this call on `stream` is this set's moe_plan
+ * (which never writes x and lets its dependents start only after its own
+ * wait), and x was written before that plan in stream order.  The library
+ * cannot check this: with any other kernel in between (one that writes x, or
+ * one launched with programmatic dependent launch that triggers its
+ * dependents early), use moe_dispatch.  Arguments and errors as moe_dispatch.
+ */
+MOE_API int moe_dispatch_after_plan(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream);
 
 /*
  * Identity experts (test stand-in for the expert FFNs): for rows r < T*k,
@@ -265,8 +296,15 @@ MOE_API int moe_step_host(moe_pool* pool, const float* h_logits, const uint16_t*
  *     of up to 512 tokens take the cluster plan, which keeps its scratch in
  *     shared memory and does not touch the array, where the device launches
  *     clusters (not with MOE_PLAN_NO_CLUSTER=1).
- *   - The first call on each device looks up the array's device address with
- *     that device current; make it before any stream capture begins.
+ *     Where the device refuses the cluster launch, such a batch silently
+ *     takes the three-launch plan, which does use the array.
+ *   - The first call on each device (and again after the device's context is
+ *     destroyed and re-created, e.g. by cudaDeviceReset) looks up the array's
+ *     device address with that device current; make it before any stream
+ *     capture begins.
+ *   - Argument checks do not depend on T (except that logits may be NULL
+ *     when T = 0): an empty batch passes the same checks and then only zeroes
+ *     counts and offsets.
  */
 MOE_API int moe_plan_static(const float* logits, int32_t T, int32_t E, int32_t P, int32_t k,
                             const int32_t* rep_off, const int32_t* rep_ids, int32_t* topk_e,
@@ -274,7 +312,9 @@ MOE_API int moe_plan_static(const float* logits, int32_t T, int32_t E, int32_t P
                             int32_t* slot, int32_t* src_token, int32_t* src_k, int32_t* error_word,
                             void* stream);
 
-/* Static string for a moe_status value. */
+/* Static string for a moe_status value, the status of the pool calls above
+ * (write-up, "FusedDispatch and FusedCombine": "Double-Buffered Static
+ * Pre-allocation"). */
 MOE_API const char* moe_status_str(int status);
 
 #ifdef __cplusplus

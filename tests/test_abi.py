@@ -125,6 +125,47 @@ def test_calls_rejected_before_launch(L):
     L.moe_pool_destroy(h)
 
 
+def test_dispatch_after_plan_checks_like_dispatch(L):
+    h, _ = _fake_pool(L)
+    good = ctypes.c_void_p(1 << 41)
+    odd = ctypes.c_void_p((1 << 41) + 4)
+    for fn in (L.moe_dispatch, L.moe_dispatch_after_plan):
+        assert fn(h, good, 8, 0, None) == -9    # no plan on this set
+        assert fn(h, odd, 8, 0, None) == -3
+        assert fn(h, None, 8, 0, None) == -1
+        assert fn(h, good, 8, 2, None) == -4
+        assert fn(h, good, 65, 0, None) == -2
+        assert fn(None, good, 8, 0, None) == -1
+    L.moe_pool_destroy(h)
+
+
+@pytest.mark.parametrize("T", [0, 1, 96])
+def test_plan_static_checks_do_not_depend_on_T(L, T):
+    """Every argument check of moe_plan_static runs before the empty-batch
+    branch: with no GPU here, a call that got past the checks could only
+    fail with MOE_ERR_CUDA (-6), so these codes come from the checks."""
+    p = ctypes.c_void_p(1 << 41)
+    odd = ctypes.c_void_p((1 << 41) + 4)
+    f = L.moe_plan_static
+
+    def call(logits=p, E=8, P=8, k=2, ro=None, ri=None, counts=p, offsets=p):
+        return f(logits, T, E, P, k, ro, ri, p, p, p, counts, offsets, p, p, p, p, None)
+
+    assert call(P=6) == -2                      # P < E
+    assert call(E=0) == -2
+    assert call(k=9) == -2                      # k > E
+    assert call(P=10) == -8                     # P > E needs a replica map
+    assert call(ro=p) == -1                     # half a replica map
+    assert call(P=10, ro=odd, ri=p) == -3       # misaligned map
+    assert call(counts=None) == -1
+    assert call(offsets=odd) == -3
+    assert f(p, -1, 8, 8, 2, None, None, p, p, p, p, p, p, p, p, p, None) == -2
+    if T == 0:
+        assert call(logits=None) == -6          # an empty batch needs no logits: it reaches the memset
+    else:
+        assert call(logits=None) == -1
+
+
 def test_replica_map_needed_when_P_exceeds_E(L):
     h, _ = _fake_pool(L, E=8, P=10)
     assert L.moe_plan(h, ctypes.c_void_p(1 << 41), 8, None, None, 0, None) == -8

@@ -3,7 +3,9 @@ memory (a graph replayed from elsewhere, a plugin whose host framework owns
 every allocation, a process that must not grow its footprint after start-up).
 
 Its results must equal moe_plan's on the same inputs, on two calls in a row
-(the second call reuses the shared scratch array the first one left behind).
+(the second call reuses the shared scratch array the first one left behind),
+and the oracle's: bit-exact ids, counts, offsets, slots and inverse maps,
+gates within 1 fp32 ulp.
 Collected last on purpose, so that a stop-at-first-failure run has already
 run every other test; it also passes alone in a fresh process.
 """
@@ -13,9 +15,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_moe_plan_gb300 import moe
 from combine_moe_plan_gb300 import workloads as wl
-from tests.gpu_util import assert_gates_close, dev, ensure_built
+from tests.gpu_util import assert_gates_close, compare_plan, dev, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +59,9 @@ def test_plan_static_matches_plan_two_calls_in_a_row():
     torch.cuda.synchronize()
     for w, got, ref in zip(cases, gots, refs):
         _compare(got, ref, w.name)
+        inp = wl.make_inputs(w, with_expert_out=False)
+        orc = oracle.plan(inp["logits"], w.k, inp["rep_off"], inp["rep_ids"], w.P)
+        compare_plan({k: v.cpu().numpy() for k, v in got.items()}, orc, f"{w.name} vs oracle")
 
 
 def test_plan_static_small_batches_overlap_on_two_streams():
@@ -65,6 +71,14 @@ def test_plan_static_small_batches_overlap_on_two_streams():
     synchronization between the streams)."""
     ensure_built()
     ws = [wl.WORKLOADS["t96_h7168_e256_k8"], wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 300)]
+    # Only the cluster plan keeps its scratch out of the shared array.  At 300
+    # tokens it is one launch; the fallback a refused cluster takes is three.
+    w300 = ws[1]
+    inp300 = wl.make_inputs(w300, with_expert_out=False)
+    probe = moe.Pool(w300.T, w300.H, w300.E, w300.P, w300.k, n_sets=1)
+    probe.plan(dev(inp300["logits"]), dev(inp300["rep_off"]), dev(inp300["rep_ids"]))
+    if probe.launches() != 1:
+        pytest.skip("this device does not take the cluster plan; overlapping calls would share the array")
     args, refs = [], []
     for w in ws:
         inp = wl.make_inputs(w, with_expert_out=False)
