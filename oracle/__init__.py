@@ -10,7 +10,10 @@ Every step follows the CloudMatrix384 write-up, section "FusedDispatch and
 FusedCombine" (routing metadata, early INT8 quantization with a scale,
 token-level load -> quantize/address -> write, expert output return), with the
 placement order of the StrataCL analysis, section 3.5 (token placement ->
-expert-window aggregation).
+expert-window aggregation).  The expert-parallel split over R ranks
+(``moe_oracle_ep.c``: ownership, receive layout, pull exchanges, and the
+transfer schedule of section 3.5 -- peer-window partition into units, LPT
+under a per-peer fan-out cap) is wrapped by the ``ep_*`` functions below.
 """
 from __future__ import annotations
 
@@ -23,6 +26,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
+_SRC_EP = os.path.join(_HERE, "moe_oracle_ep.c")
 _LIBDIR = os.path.join(_HERE, "_lib")
 _LIB = os.path.join(_LIBDIR, "libmoe_oracle.so")
 _lock = threading.Lock()
@@ -43,11 +47,12 @@ def build(force: bool = False) -> str:
     """Compile moe_oracle.c into a shared library (gcc, ISO C11, no FP
     contraction), with OpenMP for the per-token loops where gcc has it."""
     os.makedirs(_LIBDIR, exist_ok=True)
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_EP))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".tmp{os.getpid()}"
-        r = subprocess.run(["gcc", *_FLAGS, "-fopenmp", "-o", tmp, _SRC, "-lm"], capture_output=True)
+        r = subprocess.run(["gcc", *_FLAGS, "-fopenmp", "-o", tmp, _SRC, _SRC_EP, "-lm"], capture_output=True)
         if r.returncode != 0:  # no OpenMP runtime: the same loops, serial
-            subprocess.run(["gcc", *_FLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+            subprocess.run(["gcc", *_FLAGS, "-o", tmp, _SRC, _SRC_EP, "-lm"], check=True)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -74,6 +79,15 @@ def _load():
                       "orc_identity_experts", "orc_combine", "orc_combine_tokens"):
                 getattr(lib, f).restype = ctypes.c_int
             lib.orc_f32_to_bf16_array.restype = None
+            i64 = ctypes.c_int64
+            lib.orc_ep_owner.argtypes = [i32, i32, i32]
+            lib.orc_ep_owner.restype = i32
+            lib.orc_ep_layout.argtypes = [P, i32, i32, i32, P, P, P]
+            lib.orc_ep_gather.argtypes = [P, i64, P, i32, i32, i32, P]
+            lib.orc_ep_return.argtypes = [P, i64, P, i32, i32, i32, P]
+            lib.orc_ep_schedule.argtypes = [i32, i32, P, i32, i32, i32, P, P, P, P, i64, i32, P, P, P, P, P]
+            for f in ("orc_ep_layout", "orc_ep_gather", "orc_ep_return", "orc_ep_schedule"):
+                getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -211,3 +225,104 @@ def forward(logits, x, k, rep_off=None, rep_ids=None, P=None, ex_out=None):
     out.update(codes=codes, scales=scales, ex_out=ex_out,
                y=combine(ex_out, out["slot"], out["gates"]))
     return out
+
+
+# ------------------------------------------------- expert-parallel split --
+
+EP_UNIT = np.dtype([("peer", np.int32), ("src_row", np.int32), ("dst_row", np.int32), ("rows", np.int32)])
+
+
+def ep_owner(p, R, P) -> int:
+    """Rank that owns physical expert p: floor(p * R / P)."""
+    return int(_load().orc_ep_owner(int(p), int(R), int(P)))
+
+
+def ep_layout(counts, d):
+    """Receive layout of rank d from every rank's counts [R, P]: returns
+    (expert_off [n_d + 1], chunk_row [R, n_d]); expert_off[-1] is the number
+    of rows d receives."""
+    counts = _c(counts, np.int32)
+    R, P = counts.shape
+    n = ctypes.c_int32()
+    off = np.zeros(P + 1, np.int32)
+    chunk = np.zeros(R * P, np.int32)
+    _check(_load().orc_ep_layout(_p(counts), R, P, int(d), ctypes.byref(n), _p(off), _p(chunk)))
+    nd = n.value
+    return off[:nd + 1].copy(), chunk[:R * nd].reshape(R, nd).copy()
+
+
+def _planes(arrs):
+    arrs = [np.ascontiguousarray(a) for a in arrs]
+    ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    return arrs, ptrs
+
+
+def ep_gather(pools, counts, d):
+    """Dispatch exchange of one plane: pools[s] is rank s's plane [rows, ...]
+    (expert-major windows); returns rank d's receive plane."""
+    counts = _c(counts, np.int32)
+    R, P = counts.shape
+    arrs, ptrs = _planes(pools)
+    row_bytes = arrs[0].strides[0]
+    off, _ = ep_layout(counts, d)
+    out = np.zeros((int(off[-1]),) + arrs[0].shape[1:], arrs[0].dtype)
+    _check(_load().orc_ep_gather(ptrs, row_bytes, _p(counts), R, P, int(d), _p(out)))
+    return out
+
+
+def ep_return(recvs, counts, s, rows):
+    """Combine exchange of one plane: recvs[d] is rank d's receive plane;
+    returns rank s's pool plane with `rows` rows (rows no copy lands in are 0)."""
+    counts = _c(counts, np.int32)
+    R, P = counts.shape
+    arrs, ptrs = _planes(recvs)
+    row_bytes = arrs[0].strides[0]
+    out = np.zeros((rows,) + arrs[0].shape[1:], arrs[0].dtype)
+    _check(_load().orc_ep_return(ptrs, row_bytes, _p(counts), R, P, int(s), _p(out)))
+    return out
+
+
+def ep_schedule(direction, puller, counts, C, cap, unit_rows, alpha_ns, beta_gbs, row_bytes, max_units=None):
+    """LPT transfer schedule of one puller.  Returns dict with units (EP_UNIT
+    records grouped by core), cost [n] (ps), core_off [C+1], makespan (ps)."""
+    counts = _c(counts, np.int32)
+    R, P = counts.shape
+    if max_units is None:
+        max_units = int(R * P + counts.sum() // max(1, min(unit_rows)) + 1)
+    units = np.zeros(max_units, EP_UNIT)
+    cost = np.zeros(max_units, np.int64)
+    core_off = np.zeros(C + 1, np.int32)
+    n = ctypes.c_int32()
+    ms = ctypes.c_int64()
+    a = [np.ascontiguousarray(v, t) for v, t in ((cap, np.int32), (unit_rows, np.int32), (alpha_ns, np.int64),
+                                                 (beta_gbs, np.int64))]
+    _check(_load().orc_ep_schedule(int(direction), int(puller), _p(counts), R, P, int(C), *[_p(v) for v in a],
+                                   int(row_bytes), int(max_units), _p(units), _p(cost), ctypes.byref(n),
+                                   _p(core_off), ctypes.byref(ms)))
+    return {"units": units[:n.value].copy(), "cost": cost[:n.value].copy(), "core_off": core_off,
+            "makespan": ms.value}
+
+
+def ep_forward(logits_list, x_list, k, P=None, rep_off=None, rep_ids=None, recv_ex_out=None):
+    """The whole path split over R = len(logits_list) ranks: each rank plans
+    and dispatches its own batch into its own pool, the owners gather their
+    experts' rows (codes and scales), the experts run on the receive buffers
+    (identity experts unless recv_ex_out[d] gives bf16 rows), the rows return
+    to their sources, and each rank combines its own tokens.  Returns a dict
+    with per-rank lists: plan, codes, scales, counts [R, P], recv_codes,
+    recv_scales, recv_ex_out, ex_out (returned rows), y."""
+    R = len(logits_list)
+    E = logits_list[0].shape[1]
+    P = E if P is None else P
+    plans = [plan(lg, k, rep_off, rep_ids, P) for lg in logits_list]
+    disp = [dispatch(x, pl["slot"]) for x, pl in zip(x_list, plans)]
+    counts = np.stack([pl["counts"] for pl in plans])
+    recv_codes = [ep_gather([c for c, _ in disp], counts, d) for d in range(R)]
+    recv_scales = [ep_gather([s for _, s in disp], counts, d) for d in range(R)]
+    if recv_ex_out is None:
+        recv_ex_out = [identity_experts(c, s) for c, s in zip(recv_codes, recv_scales)]
+    ex_out = [ep_return(recv_ex_out, counts, s, int(plans[s]["offsets"][-1])) for s in range(R)]
+    y = [combine(ex_out[s], plans[s]["slot"], plans[s]["gates"]) for s in range(R)]
+    return {"plan": plans, "codes": [c for c, _ in disp], "scales": [s for _, s in disp], "counts": counts,
+            "recv_codes": recv_codes, "recv_scales": recv_scales, "recv_ex_out": recv_ex_out,
+            "ex_out": ex_out, "y": y}

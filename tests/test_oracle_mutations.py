@@ -83,7 +83,7 @@ MUTATIONS = [
 def _copy_tree(dst: str) -> None:
     """The oracle, the pin tests and what they import, without build output."""
     os.makedirs(os.path.join(dst, "oracle"))
-    for f in ("__init__.py", "moe_oracle.c"):
+    for f in ("__init__.py", "moe_oracle.c", "moe_oracle_ep.c"):
         shutil.copy(os.path.join(ROOT, "oracle", f), os.path.join(dst, "oracle", f))
     os.makedirs(os.path.join(dst, "combine_moe_plan_gb300"))
     for f in ("__init__.py", "workloads.py"):
