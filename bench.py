@@ -64,6 +64,8 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
+    ap.add_argument("--ep-ranks", type=int, default=8,
+                    help="ranks of the expert-parallel split emulated on this GPU (0: skip that phase)")
     return ap.parse_args()
 
 
@@ -552,6 +554,12 @@ def run_ours(a, w: wl.Workload):
     # ---- phase D: decode-batch latency (CUDA graphs) ----
     decode = None if a.no_e2e else decode_latency(dev)
 
+    # ---- phase E: the expert-parallel split, R ranks emulated on this GPU ----
+    split = None
+    if a.ep_ranks > 0 and ws == 1 and not a.no_e2e:
+        torch.cuda.empty_cache()
+        split = ep_split(dev, w, a.ep_ranks)
+
     # ---- max over ranks ----
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev)
     if rank == 0:
@@ -608,6 +616,7 @@ def run_ours(a, w: wl.Workload):
             "gpu_launches": int(launches),
             "clocks": clocks,
             "decode_latency": decode,
+            "ep_split_emulated": split,
         }
         if not a.no_cpu_baseline and ws == 1:
             out["cpu_baseline"] = cpu_baseline(w, inp)
@@ -615,6 +624,96 @@ def run_ours(a, w: wl.Workload):
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def ep_split(dev, w, R, reps=20, n_b2b=20):
+    """The expert-parallel split of the workload over R ranks emulated on this
+    GPU (each rank its own seeded batch of w.T tokens, its own pool and a
+    worst-case receive buffer): per step every rank plans and dispatches, the
+    counts come to the host, libmoe's host scheduler makes both exchanges'
+    LPT schedules for all R pullers, the dispatch pull (one launch, all
+    pullers), the expert outputs (synthetic bf16 rows already resident in the
+    receive buffers), the combine pull, and every rank's combine; the host
+    schedules while the dispatch kernels run.  Reports the
+    step time (tokens of all ranks per second), the two pull kernels' mean
+    durations back to back with the bytes they move (read + write) against
+    the HBM copy peak, and the host scheduling time."""
+    import torch
+    from combine_moe_plan_gb300 import ep
+    g = ep.EmulatedGroup(R, w.T, w.H, w.E, w.P, w.k, device=dev)
+    inps = [wl.make_inputs(w, seed=r, with_expert_out=False) for r in range(R)]
+    logits = [torch.from_numpy(i["logits"]).to(dev) for i in inps]
+    xs = [torch.from_numpy(i["x"].view(np.int16)).to(dev).view(torch.bfloat16) for i in inps]
+    ro = None if inps[0]["rep_off"] is None else torch.from_numpy(inps[0]["rep_off"]).to(dev)
+    ri = None if inps[0]["rep_ids"] is None else torch.from_numpy(inps[0]["rep_ids"]).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    for t in g.recv_ex:
+        t.copy_(torch.randn(t.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16))
+    s = torch.cuda.current_stream(dev)
+    sched_s = []
+
+    def one_step():
+        ev = g.plan_dispatch(logits, xs, ro, ri)
+        counts = g.counts_host(ev)
+        t0 = time.perf_counter()
+        disp, comb, recv_rows = g.schedules(counts)
+        sched_s.append(time.perf_counter() - t0)
+        du, dc = g.upload(disp)
+        cu, cc = g.upload(comb)
+        g.pull_dispatch(du, dc)
+        g.pull_combine(cu, cc)
+        g.combine([w.T] * R)
+        return (du, dc, cu, cc), recv_rows, counts
+
+    for _ in range(3):
+        one_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sched_s.clear()
+    e0.record(s)
+    for _ in range(reps):
+        packed, recv_rows, counts = one_step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    step_ms = e0.elapsed_time(e1) / reps
+
+    du, dc, cu, cc = packed
+    b2b = {}
+    for name, fn in (("dispatch_pull", lambda: g.pull_dispatch(du, dc)),
+                     ("combine_pull", lambda: g.pull_combine(cu, cc))):
+        for _ in range(3):
+            fn()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(s)
+        for _ in range(n_b2b):
+            fn()
+        a1.record(s)
+        torch.cuda.synchronize()
+        b2b[name] = a0.elapsed_time(a1) * 1e3 / n_b2b
+    if g.check() != 0:
+        raise RuntimeError("device error word set in the split pass")
+    rows = int(sum(recv_rows))
+    moved = {"dispatch_pull": 2 * rows * (w.H + 4 * g.Gs), "combine_pull": 2 * rows * 2 * w.H}
+    peak, peak_src = _peaks()
+    out = {"ranks": R, "workload_per_rank": w.name, "cores_per_puller": g.cores,
+           "desc": {"fanout_cap": list(g.desc.fanout_cap), "unit_rows": list(g.desc.unit_rows),
+                    "alpha_ns": list(g.desc.alpha_ns), "beta_gbs": list(g.desc.beta_gbs)},
+           "value": R * w.T / (step_ms * 1e-3), "unit": "tokens/s (all ranks)", "ms_per_step": step_ms,
+           "host_schedule_ms_per_step": 1e3 * statistics.median(sched_s),
+           "rows_exchanged": rows, "kernel_us_back_to_back": b2b,
+           "pull_roofline": {k: {"bytes": moved[k], "achieved_gbs": moved[k] / (b2b[k] * 1e-6) / 1e9,
+                                 "peak": peak, "frac": moved[k] / (b2b[k] * 1e-6) / 1e9 / peak}
+                             for k in b2b},
+           "peak_source": peak_src,
+           "note": "all ranks on one GPU: both exchanges move every rank's rows through local HBM (one launch "
+                   "for all pullers); the step includes the counts' device-to-host copy and the host "
+                   "schedules; unmeasured across GPUs"}
+    del g
+    torch.cuda.empty_cache()
+    return out
 
 
 E2E_SETS = 3

@@ -1,0 +1,405 @@
+// ep.cu -- the expert-parallel split of the pool over R ranks: ownership,
+// receive layout, the transfer schedule (host), and the pull exchange
+// (device).
+//
+// StrataCL analysis, section 3.5 (Workload-balanced NPU-core Partitioning):
+// token placement -> expert-window aggregation -> peer-window partition; each
+// peer's payload cut into transfer units of at most S_t rows, unit cost
+// alpha_t + bytes / beta_t per tier, min-makespan under a per-peer fan-out cap
+// per stripe, solved by an LPT-style list scheduler that outputs a task list
+// per core.  Section 3.4 (Full-mesh): a collective is a set of remote-slice
+// tuples <peer, src, dst, bytes>; data-movement collectives pull -- each rank
+// reads remote slices into its own buffer, no producer-consumer handshake.
+//
+// GPU mapping of the pull: one CTA per (core, puller); a core walks its unit
+// list in order, and every thread of the CTA streams its share of each
+// unit's contiguous byte range with 16-byte loads (four in flight per thread)
+// and 16-byte stores.  A unit is one contiguous run of rows in both buffers
+// (a piece of one peer's window of one expert), so a plane of a unit is a
+// plain memcpy; the schedule decides which core moves what, in which order.
+#include <algorithm>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "moe_ep.h"
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+// First expert of rank d: the smallest p with floor(p * R / P) >= d, i.e.
+// ceil(d * P / R).
+inline int32_t rank_first_expert(int32_t d, int32_t R, int32_t P) {
+    return (int32_t)(((int64_t)d * P + R - 1) / R);
+}
+
+inline int32_t expert_owner(int32_t p, int32_t R, int32_t P) { return (int32_t)(((int64_t)p * R) / P); }
+
+int check_group(int32_t R, int32_t P) {
+    if (R < 1 || R > MOE_EP_MAX_RANKS || P < 1 || P > 4096) return MOE_ERR_SIZE;
+    return MOE_OK;
+}
+
+int check_desc(const moe_ep_desc* d) {
+    if (d == nullptr) return MOE_ERR_NULL;
+    int rc = check_group(d->R, d->P);
+    if (rc != MOE_OK) return rc;
+    if (d->cores < 1 || d->cores > 4096) return MOE_ERR_SIZE;
+    for (int t = 0; t < 2; ++t)
+        if (d->fanout_cap[t] < 1 || d->unit_rows[t] < 1 || d->unit_rows[t] > (1 << 20) || d->alpha_ns[t] < 0 ||
+            d->alpha_ns[t] > ((int64_t)1 << 40) || d->beta_gbs[t] < 1)
+            return MOE_ERR_SIZE;
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- pull ----
+
+constexpr int kPullThreads = 512;
+constexpr int kPullUnroll = 4;  // 16-byte loads in flight per thread
+
+struct PullPlanes {
+    const char* src[2][MOE_EP_MAX_RANKS];
+    char* dst[2][MOE_EP_MAX_RANKS];
+    int64_t src_rows[2][MOE_EP_MAX_RANKS];
+    int64_t dst_rows[2][MOE_EP_MAX_RANKS];
+    int64_t row_bytes[2];
+    int32_t n_planes;
+};
+
+// Copy n16 16-byte words from src to dst with the whole CTA.
+__device__ __forceinline__ void cta_copy16(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n16) {
+    constexpr int64_t kStep = (int64_t)kPullThreads * kPullUnroll;
+    int64_t j = threadIdx.x;
+    for (; j + (kPullUnroll - 1) * kPullThreads < n16; j += kStep) {
+        uint4 v[kPullUnroll];
+#pragma unroll
+        for (int u = 0; u < kPullUnroll; ++u) v[u] = ld_stream16(src + j + u * kPullThreads);
+#pragma unroll
+        for (int u = 0; u < kPullUnroll; ++u) st16(dst + j + u * kPullThreads, v[u]);
+    }
+    for (; j < n16; j += kPullThreads) st16(dst + j, ld_stream16(src + j));
+}
+
+__global__ void __launch_bounds__(kPullThreads)
+ep_pull_kernel(const moe_ep_unit* __restrict__ units, const int32_t* __restrict__ core_off, int32_t n_units,
+               int32_t R, int32_t C, int32_t first_puller, const PullPlanes pl, int32_t* __restrict__ err) {
+    grid_dependency_sync();
+    allow_dependents();
+    const int c = blockIdx.x;
+    const int i = blockIdx.y;
+    const int r = first_puller + i;
+    const int32_t* co = core_off + (size_t)i * (C + 1);
+    const int32_t b = co[c], e = co[c + 1];
+    if (b < 0 || e > n_units || b > e) {
+        if (threadIdx.x == 0) set_error(err, MOE_DEVERR_UNIT);
+        return;
+    }
+    for (int32_t k = b; k < e; ++k) {
+        const moe_ep_unit u = units[k];
+        bool ok = u.peer >= 0 && u.peer < R && u.rows >= 0 && u.src_row >= 0 && u.dst_row >= 0;
+        for (int p = 0; p < pl.n_planes && ok; ++p)
+            ok = (int64_t)u.src_row + u.rows <= pl.src_rows[p][u.peer] &&
+                 (int64_t)u.dst_row + u.rows <= pl.dst_rows[p][r] &&
+                 (u.rows == 0 || (pl.src[p][u.peer] != nullptr && pl.dst[p][r] != nullptr));
+        if (!ok) {  // uniform over the CTA: every thread read the same unit
+            if (threadIdx.x == 0) set_error(err, MOE_DEVERR_UNIT);
+            continue;
+        }
+        for (int p = 0; p < pl.n_planes; ++p) {
+            const int64_t rb = pl.row_bytes[p];
+            cta_copy16(reinterpret_cast<const uint4*>(pl.src[p][u.peer] + (int64_t)u.src_row * rb),
+                       reinterpret_cast<uint4*>(pl.dst[p][r] + (int64_t)u.dst_row * rb), (int64_t)u.rows * rb / 16);
+        }
+    }
+}
+
+// ------------------------------------------------------------ schedule ----
+
+// Window starts of every rank from the counts.  pool[s * (P + 1) + p]: expert
+// p's first row in rank s's pool (the plan's exclusive scan); recv[s * P + p]:
+// s's first row of expert p in its owner's receive buffer.
+struct Windows {
+    int32_t R = 0, P = 0;
+    std::vector<int64_t> pool, recv;
+
+    int build(int32_t R_, int32_t P_, const int32_t* counts) {
+        R = R_;
+        P = P_;
+        pool.assign((size_t)R * (P + 1), 0);
+        recv.assign((size_t)R * P, 0);
+        for (int32_t s = 0; s < R; ++s) {
+            int64_t acc = 0;
+            for (int32_t p = 0; p < P; ++p) {
+                pool[(size_t)s * (P + 1) + p] = acc;
+                acc += counts[(size_t)s * P + p];
+            }
+            pool[(size_t)s * (P + 1) + P] = acc;
+            if (acc > INT32_MAX) return MOE_ERR_SIZE;
+        }
+        for (int32_t d = 0; d < R; ++d) {
+            int64_t row = 0;
+            for (int32_t p = rank_first_expert(d, R, P); p < rank_first_expert(d + 1, R, P); ++p)
+                for (int32_t s = 0; s < R; ++s) {
+                    recv[(size_t)s * P + p] = row;
+                    row += counts[(size_t)s * P + p];
+                }
+            if (row > INT32_MAX) return MOE_ERR_SIZE;
+        }
+        return MOE_OK;
+    }
+};
+
+struct Schedule {
+    std::vector<moe_ep_unit> units;  // grouped by core, each core's list in assignment order
+    std::vector<int32_t> core_off;   // [C + 1]
+    int64_t makespan = 0;
+};
+
+int check_schedule_args(const moe_ep_desc* desc, int32_t direction, const int32_t* counts, int64_t row_bytes,
+                        int32_t max_units) {
+    int rc = check_desc(desc);
+    if (rc != MOE_OK) return rc;
+    if ((direction != 0 && direction != 1) || row_bytes < 1 || row_bytes > ((int64_t)1 << 24) || max_units < 0)
+        return MOE_ERR_SIZE;
+    for (size_t i = 0; i < (size_t)desc->R * desc->P; ++i)
+        if (counts[i] < 0) return MOE_ERR_SIZE;
+    return MOE_OK;
+}
+
+// The schedule of one puller: units in ascending destination row with their
+// costs (ps), longest first (equal costs in that order), each to the
+// least-loaded eligible core (equal loads: the lower core) under the fan-out
+// cap.
+void schedule_one(const moe_ep_desc& desc, const Windows& w, const int32_t* counts, int32_t direction,
+                  int32_t puller, int64_t row_bytes, Schedule* out) {
+    const int32_t R = desc.R, P = desc.P, C = desc.cores;
+    std::vector<moe_ep_unit> u;
+    std::vector<int64_t> cost;
+    auto cut = [&](int32_t peer, int64_t src0, int64_t dst0, int64_t n) {
+        const int t = peer == puller ? 0 : 1;
+        const int64_t S = desc.unit_rows[t];
+        for (int64_t at = 0; at < n; at += S) {
+            const int64_t rows = std::min(S, n - at);
+            u.push_back(moe_ep_unit{peer, (int32_t)(src0 + at), (int32_t)(dst0 + at), (int32_t)rows});
+            cost.push_back(desc.alpha_ns[t] * 1000 + rows * row_bytes * 1000 / desc.beta_gbs[t]);
+        }
+    };
+    if (direction == 0) {
+        for (int32_t p = rank_first_expert(puller, R, P); p < rank_first_expert(puller + 1, R, P); ++p)
+            for (int32_t s = 0; s < R; ++s)
+                cut(s, w.pool[(size_t)s * (P + 1) + p], w.recv[(size_t)s * P + p], counts[(size_t)s * P + p]);
+    } else {
+        for (int32_t p = 0; p < P; ++p)
+            cut(expert_owner(p, R, P), w.recv[(size_t)puller * P + p], w.pool[(size_t)puller * (P + 1) + p],
+                counts[(size_t)puller * P + p]);
+    }
+    const int32_t nu = (int32_t)u.size();
+    struct Key {
+        int64_t cost;
+        int32_t idx;
+    };
+    std::vector<Key> order(nu);
+    for (int32_t k = 0; k < nu; ++k) order[k] = Key{cost[k], k};
+    std::sort(order.begin(), order.end(),
+              [](const Key& a, const Key& b) { return a.cost != b.cost ? a.cost > b.cost : a.idx < b.idx; });
+
+    // Cores sit in a binary heap by (load, core); a unit takes the first
+    // eligible core popped, i.e. the least-loaded eligible core with ties to
+    // the lower core.  A core with the longest list is always eligible (its
+    // next stripe is still empty), so the search ends.
+    std::vector<int64_t> load(C, 0);
+    std::vector<int32_t> len(C, 0), core_of(nu), pos(nu);
+    std::vector<int32_t> stripe;  // stripe[i * R + q]: cores whose i-th unit is from peer q
+    auto above = [&](int32_t a, int32_t b) { return load[a] != load[b] ? load[a] > load[b] : a > b; };
+    std::vector<int32_t> heap(C), held;
+    for (int32_t c = 0; c < C; ++c) heap[c] = c;
+    std::make_heap(heap.begin(), heap.end(), above);
+    for (int32_t k = 0; k < nu; ++k) {
+        const int32_t i = order[k].idx;
+        const int32_t q = u[i].peer;
+        const int32_t cap = desc.fanout_cap[q == puller ? 0 : 1];
+        held.clear();
+        int32_t best = -1;
+        while (best < 0) {
+            std::pop_heap(heap.begin(), heap.end(), above);
+            const int32_t c = heap.back();
+            heap.pop_back();
+            const size_t at = (size_t)len[c] * R + q;
+            if (at >= stripe.size() || stripe[at] < cap)
+                best = c;
+            else
+                held.push_back(c);
+        }
+        const size_t at = (size_t)len[best] * R + q;
+        if (at >= stripe.size()) stripe.resize(((size_t)len[best] + 1) * R * 2, 0);
+        stripe[at] += 1;
+        core_of[i] = best;
+        pos[i] = len[best];
+        len[best] += 1;
+        load[best] += cost[i];
+        held.push_back(best);
+        for (int32_t c : held) {
+            heap.push_back(c);
+            std::push_heap(heap.begin(), heap.end(), above);
+        }
+    }
+    out->core_off.assign(C + 1, 0);
+    for (int32_t c = 0; c < C; ++c) out->core_off[c + 1] = out->core_off[c] + len[c];
+    out->units.resize(nu);
+    for (int32_t i = 0; i < nu; ++i) out->units[out->core_off[core_of[i]] + pos[i]] = u[i];
+    out->makespan = nu ? *std::max_element(load.begin(), load.end()) : 0;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+MOE_API int moe_ep_experts(int32_t R, int32_t P, int32_t d, int32_t* first, int32_t* count) {
+    if (first == nullptr || count == nullptr) return MOE_ERR_NULL;
+    int rc = check_group(R, P);
+    if (rc != MOE_OK) return rc;
+    if (d < 0 || d >= R) return MOE_ERR_SIZE;
+    *first = rank_first_expert(d, R, P);
+    *count = rank_first_expert(d + 1, R, P) - *first;
+    return MOE_OK;
+}
+
+MOE_API int moe_ep_layout(int32_t R, int32_t P, const int32_t* counts, int32_t d, int32_t* expert_off,
+                          int32_t* chunk_row) {
+    if (counts == nullptr || expert_off == nullptr || chunk_row == nullptr) return MOE_ERR_NULL;
+    int32_t lo = 0, nd = 0;
+    int rc = moe_ep_experts(R, P, d, &lo, &nd);
+    if (rc != MOE_OK) return rc;
+    int64_t row = 0;
+    for (int32_t i = 0; i < nd; ++i) {
+        expert_off[i] = (int32_t)row;
+        for (int32_t s = 0; s < R; ++s) {
+            chunk_row[(size_t)s * nd + i] = (int32_t)row;
+            const int32_t n = counts[(size_t)s * P + lo + i];
+            if (n < 0) return MOE_ERR_SIZE;
+            row += n;
+            if (row > INT32_MAX) return MOE_ERR_SIZE;
+        }
+    }
+    expert_off[nd] = (int32_t)row;
+    return MOE_OK;
+}
+
+MOE_API int moe_ep_max_units(const moe_ep_desc* desc, int64_t rows, int32_t* max_units) {
+    if (max_units == nullptr) return MOE_ERR_NULL;
+    int rc = check_desc(desc);
+    if (rc != MOE_OK) return rc;
+    if (rows < 0) return MOE_ERR_SIZE;
+    const int64_t smin = std::min(desc->unit_rows[0], desc->unit_rows[1]);
+    const int64_t nd_max = (desc->P + desc->R - 1) / desc->R;  // the largest block of experts
+    const int64_t n = rows / smin + (int64_t)desc->R * nd_max;
+    if (n > INT32_MAX) return MOE_ERR_SIZE;
+    *max_units = (int32_t)n;
+    return MOE_OK;
+}
+
+MOE_API int moe_ep_schedule(const moe_ep_desc* desc, int32_t direction, int32_t puller, const int32_t* counts,
+                            int64_t row_bytes, moe_ep_unit* units, int32_t max_units, int32_t* n_units,
+                            int32_t* core_off, int64_t* makespan_ps) {
+    if (counts == nullptr || units == nullptr || n_units == nullptr || core_off == nullptr) return MOE_ERR_NULL;
+    int rc = check_schedule_args(desc, direction, counts, row_bytes, max_units);
+    if (rc != MOE_OK) return rc;
+    if (puller < 0 || puller >= desc->R) return MOE_ERR_SIZE;
+    Windows win;
+    if ((rc = win.build(desc->R, desc->P, counts)) != MOE_OK) return rc;
+    Schedule out;
+    schedule_one(*desc, win, counts, direction, puller, row_bytes, &out);
+    if ((int64_t)out.units.size() > max_units) return MOE_ERR_SIZE;
+    std::copy(out.units.begin(), out.units.end(), units);
+    std::copy(out.core_off.begin(), out.core_off.end(), core_off);
+    *n_units = (int32_t)out.units.size();
+    if (makespan_ps != nullptr) *makespan_ps = out.makespan;
+    return MOE_OK;
+}
+
+MOE_API int moe_ep_schedule_group(const moe_ep_desc* desc, int32_t direction, const int32_t* counts,
+                                  int64_t row_bytes, moe_ep_unit* units, int32_t max_units, int32_t* n_units,
+                                  int32_t* core_off, int64_t* makespan_ps) {
+    if (counts == nullptr || units == nullptr || n_units == nullptr || core_off == nullptr) return MOE_ERR_NULL;
+    int rc = check_schedule_args(desc, direction, counts, row_bytes, max_units);
+    if (rc != MOE_OK) return rc;
+    const int32_t R = desc->R, C = desc->cores;
+    Windows win;
+    if ((rc = win.build(R, desc->P, counts)) != MOE_OK) return rc;
+    std::vector<Schedule> out((size_t)R);
+    // One puller per worker thread; each writes only its own Schedule.
+    const int32_t n_thr = std::max(1, std::min<int32_t>(R, (int32_t)std::thread::hardware_concurrency()));
+    auto work = [&](int32_t first) {
+        for (int32_t r = first; r < R; r += n_thr) schedule_one(*desc, win, counts, direction, r, row_bytes, &out[r]);
+    };
+    std::vector<std::thread> pool;
+    for (int32_t t = 1; t < n_thr; ++t) pool.emplace_back(work, t);
+    work(0);
+    for (auto& t : pool) t.join();
+    int64_t total = 0;
+    for (const Schedule& sc : out) total += (int64_t)sc.units.size();
+    if (total > max_units) return MOE_ERR_SIZE;
+    int32_t base = 0;
+    for (int32_t r = 0; r < R; ++r) {
+        std::copy(out[r].units.begin(), out[r].units.end(), units + base);
+        for (int32_t c = 0; c <= C; ++c) core_off[(size_t)r * (C + 1) + c] = base + out[r].core_off[c];
+        if (makespan_ps != nullptr) makespan_ps[r] = out[r].makespan;
+        base += (int32_t)out[r].units.size();
+    }
+    *n_units = base;
+    return MOE_OK;
+}
+
+MOE_API int moe_ep_pull(const moe_ep_unit* units, const int32_t* core_off, int32_t n_units, int32_t R,
+                        int32_t cores, int32_t first_puller, int32_t n_pullers, const moe_ep_plane* planes,
+                        int32_t n_planes, int32_t* error_word, void* stream) {
+    if (core_off == nullptr || planes == nullptr || error_word == nullptr) return MOE_ERR_NULL;
+    if (units == nullptr && n_units > 0) return MOE_ERR_NULL;
+    if (R < 1 || R > MOE_EP_MAX_RANKS || cores < 1 || cores > 4096 || n_pullers < 1 || first_puller < 0 ||
+        first_puller + n_pullers > R || n_planes < 1 || n_planes > 2 || n_units < 0)
+        return MOE_ERR_SIZE;
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(units) || misaligned(error_word)) return MOE_ERR_ALIGN;
+    PullPlanes pl;
+    std::memset(&pl, 0, sizeof(pl));
+    pl.n_planes = n_planes;
+    for (int p = 0; p < n_planes; ++p) {
+        const moe_ep_plane& a = planes[p];
+        if (a.row_bytes < 16 || a.row_bytes % 16 != 0) return MOE_ERR_SIZE;
+        pl.row_bytes[p] = a.row_bytes;
+        for (int q = 0; q < R; ++q) {
+            if (a.src_rows[q] < 0 || a.dst_rows[q] < 0) return MOE_ERR_SIZE;
+            if (misaligned(a.src[q]) || misaligned(a.dst[q])) return MOE_ERR_ALIGN;
+            pl.src[p][q] = static_cast<const char*>(a.src[q]);
+            pl.dst[p][q] = static_cast<char*>(a.dst[q]);
+            pl.src_rows[p][q] = a.src[q] == nullptr ? 0 : a.src_rows[q];
+            pl.dst_rows[p][q] = a.dst[q] == nullptr ? 0 : a.dst_rows[q];
+        }
+    }
+    cudaError_t e = launch_pdl(ep_pull_kernel, dim3((unsigned)cores, (unsigned)n_pullers), dim3(kPullThreads), 0,
+                               static_cast<cudaStream_t>(stream), units, core_off, n_units, R, cores,
+                               first_puller, pl, error_word);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+MOE_API int moe_dequant_rows(const int8_t* codes, const float* scales, int32_t rows, int32_t H,
+                             int32_t scale_stride, uint16_t* out, void* stream) {
+    if (rows < 0 || H < kGroup || H > 65536 || H % kGroup != 0 || scale_stride < H / kGroup ||
+        scale_stride % 4 != 0)
+        return MOE_ERR_SIZE;
+    if (rows == 0) return MOE_OK;
+    if (codes == nullptr || scales == nullptr || out == nullptr) return MOE_ERR_NULL;
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(codes) || misaligned(scales) || misaligned(out)) return MOE_ERR_ALIGN;
+    uint64_t launches = 0;
+    cudaError_t e = launch_identity_experts(codes, scales, rows, H, scale_stride, out,
+                                            static_cast<cudaStream_t>(stream), &launches);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

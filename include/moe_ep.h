@@ -1,0 +1,213 @@
+/*
+ * moe_ep.h -- C ABI of libmoe, part 2: the expert-parallel split of the
+ * dispatch / combine pool over R ranks.
+ *
+ * The method's real setting (CloudMatrix384 write-up, "FusedDispatch and
+ * FusedCombine"; StrataCL analysis, sections 3.4 and 3.5) spreads the
+ * experts over the ranks of an expert-parallel group.  Here:
+ *   - physical expert p lives on rank floor(p * R / P), one contiguous block
+ *     of experts per rank (moe_ep_experts);
+ *   - every rank plans and dispatches its own batch into its own pool with
+ *     moe_plan / moe_dispatch (include/moe.h): its pool is expert-major, so
+ *     the rows for rank d's experts form one contiguous peer window;
+ *   - rank d's receive buffer is expert-major over d's experts: inside expert
+ *     p's window come source rank 0's rows, then rank 1's, ..., each source's
+ *     rows in its own window order (token placement -> expert-window
+ *     aggregation -> peer-window partition, StrataCL section 3.5)
+ *     (moe_ep_layout);
+ *   - each direction is one pull exchange (StrataCL section 3.4: every rank
+ *     reads remote slices into its own buffer; no producer-consumer
+ *     handshake): receivers pull their experts' INT8 rows and scales from
+ *     the sources (dispatch), then sources pull their bf16 expert outputs
+ *     back into their own pool rows (combine), where moe_combine reduces
+ *     them in ascending j as on one GPU;
+ *   - a pull is cut into transfer units of at most S_t rows (one expert
+ *     window of one peer per unit or less), each costed tau = alpha_t +
+ *     bytes / beta_t for its tier t (0: the puller's own memory, 1: another
+ *     rank's), and list-scheduled longest first onto C cores (worker CTAs),
+ *     each unit to the least-loaded core, under the per-peer fan-out cap: in
+ *     every stripe (the i-th unit of every core's list) at most H_t cores
+ *     work on one peer (StrataCL section 3.5, min-makespan with a fairness
+ *     constraint, LPT list scheduler) (moe_ep_schedule);
+ *   - moe_ep_pull executes the units: for one puller on a real group (its
+ *     peers' buffers mapped into its address space), or for all R pullers
+ *     of a group emulated on one GPU in one launch, with every rank's
+ *     buffers in local memory.
+ *
+ * Conventions as in moe.h: 0 or a negative moe_status; arguments checked on
+ * the host before anything is launched; device pointers 16-byte aligned;
+ * every launch asynchronous on `stream`.  The host calls (experts, layout,
+ * max_units, schedule) need no GPU and allocate only host memory.
+ */
+#ifndef MOE_EP_H
+#define MOE_EP_H
+
+#include "moe.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_EP_MAX_RANKS 64
+
+/* Device error-word bit (moe_ep_pull): a unit outside its buffers or an
+ * out-of-range peer was skipped. */
+#define MOE_DEVERR_UNIT 0x8
+
+/*
+ * The expert-parallel group and its transfer cost model (StrataCL section
+ * 3.5).  Index t of the two-element arrays is the tier: 0 for units the
+ * puller reads from its own memory, 1 for units read from another rank.
+ *   R            ranks, 1 .. MOE_EP_MAX_RANKS
+ *   P            physical experts, 1 .. 4096 (a rank may own none when P < R)
+ *   cores        C, worker CTAs of one puller, 1 .. 4096
+ *   fanout_cap   H_t >= 1: cores of one puller working on one peer in one stripe
+ *   unit_rows    S_t: rows per transfer unit at most, 1 .. 2^20
+ *   alpha_ns     per-unit latency of tier t in ns, 0 .. 2^40
+ *   beta_gbs     bandwidth of tier t in GB/s (bytes per ns), >= 1
+ * Unit cost in picoseconds: alpha_ns * 1000 + floor(bytes * 1000 / beta_gbs).
+ */
+typedef struct moe_ep_desc {
+    int32_t R, P, cores;
+    int32_t fanout_cap[2];
+    int32_t unit_rows[2];
+    int64_t alpha_ns[2];
+    int64_t beta_gbs[2];
+} moe_ep_desc;
+
+/* One transfer unit (the remote-slice tuple <peer, src, dst, bytes> of
+ * StrataCL section 3.4, in rows): rows [src_row, src_row + rows) of the
+ * peer's source buffer go to rows [dst_row, dst_row + rows) of the puller's
+ * destination buffer.  16 bytes. */
+typedef struct moe_ep_unit {
+    int32_t peer, src_row, dst_row, rows;
+} moe_ep_unit;
+
+/*
+ * Experts of rank d: p in [*first, *first + *count), i.e. every p with
+ * floor(p * R / P) == d (StrataCL section 3.5, expert windows aggregated at
+ * their owner).  Host only.
+ */
+MOE_API int moe_ep_experts(int32_t R, int32_t P, int32_t d, int32_t* first, int32_t* count);
+
+/*
+ * Receive layout of rank d (StrataCL section 3.5: expert-window aggregation,
+ * peer-window partition).
+ *   counts      host int32 [R, P]: counts[s, p] = rows rank s routed to
+ *               physical expert p (each rank's moe_plan counts)
+ *   expert_off  host int32 [n_d + 1]: start row of each of d's experts in
+ *               d's receive buffer; expert_off[n_d] = rows d receives
+ *   chunk_row   host int32 [R, n_d]: start row of source s's rows of d's
+ *               i-th expert (n_d = count from moe_ep_experts)
+ * Host only.
+ */
+MOE_API int moe_ep_layout(int32_t R, int32_t P, const int32_t* counts, int32_t d, int32_t* expert_off,
+                          int32_t* chunk_row);
+
+/*
+ * An upper bound on the units one puller's schedule can hold when it moves
+ * at most `rows` rows: rows / min(S_t) + R * (experts of the largest rank).
+ * Host only.
+ */
+MOE_API int moe_ep_max_units(const moe_ep_desc* desc, int64_t rows, int32_t* max_units);
+
+/*
+ * The transfer schedule of one puller (StrataCL section 3.5).
+ *   direction  0 = dispatch: puller d pulls, from every rank s, s's rows of
+ *              d's experts (src_row in s's pool rows, dst_row in d's receive
+ *              buffer); 1 = combine: puller s pulls its rows back from every
+ *              owner d (src_row in d's receive buffer, dst_row in s's pool
+ *              rows)
+ *   counts     host int32 [R, P] as for moe_ep_layout
+ *   row_bytes  bytes one row moves (all planes together), 1 .. 2^24
+ * Units are enumerated in ascending destination row (each (peer, expert)
+ * window cut into pieces of at most S_t rows), costed, ordered by
+ * decreasing cost (equal costs in enumeration order), and assigned one by
+ * one to the least-loaded core among those whose next stripe holds fewer
+ * than H_t units of the unit's peer (equal loads: the lower core; a core
+ * with the longest list is always eligible).
+ * Outputs (host): units [*n_units] grouped by core -- core c's list, in the
+ * order assigned, is units[core_off[c] .. core_off[c+1]) -- core_off
+ * [cores + 1], and the makespan (the largest core load, ps; may be NULL).
+ * MOE_ERR_SIZE if more than max_units units are needed.  Host only.
+ */
+MOE_API int moe_ep_schedule(const moe_ep_desc* desc, int32_t direction, int32_t puller, const int32_t* counts,
+                            int64_t row_bytes, moe_ep_unit* units, int32_t max_units, int32_t* n_units,
+                            int32_t* core_off, int64_t* makespan_ps);
+
+/*
+ * The schedules of all R pullers of a group in one call (the same schedule
+ * moe_ep_schedule gives each puller), computed on up to R host threads and
+ * packed: puller r's core c runs units[core_off[r, c] .. core_off[r, c+1])
+ * with absolute indices, ready for moe_ep_pull with first_puller 0 and
+ * n_pullers R.
+ *   units        host moe_ep_unit [max_units] (all pullers together)
+ *   core_off     host int32 [R, cores + 1]
+ *   n_units      total units written
+ *   makespan_ps  host int64 [R] (may be NULL)
+ * MOE_ERR_SIZE if more than max_units units are needed in total (R times
+ * moe_ep_max_units for the group's total rows always suffices).  Host only.
+ */
+MOE_API int moe_ep_schedule_group(const moe_ep_desc* desc, int32_t direction, const int32_t* counts,
+                                  int64_t row_bytes, moe_ep_unit* units, int32_t max_units, int32_t* n_units,
+                                  int32_t* core_off, int64_t* makespan_ps);
+
+/*
+ * One plane of a pull (INT8 codes, fp32 scales or bf16 rows): where the
+ * plane lives in every rank's source and destination buffer.
+ *   src[q], src_rows[q]  device address and row count of peer q's source
+ *                        buffer (q < R)
+ *   dst[r], dst_rows[r]  device address and row count of puller r's
+ *                        destination buffer (r < R)
+ *   row_bytes            bytes per row, a multiple of 16
+ * Entries of ranks that take no part may be NULL with 0 rows.
+ */
+typedef struct moe_ep_plane {
+    const void* src[MOE_EP_MAX_RANKS];
+    void* dst[MOE_EP_MAX_RANKS];
+    int64_t src_rows[MOE_EP_MAX_RANKS];
+    int64_t dst_rows[MOE_EP_MAX_RANKS];
+    int64_t row_bytes;
+} moe_ep_plane;
+
+/*
+ * Execute the schedules of pullers first_puller .. first_puller + n_pullers - 1
+ * in one launch (pull mode, StrataCL section 3.4): CTA (c, i) runs core c of
+ * puller first_puller + i, its units in list order, copying every plane of
+ * each unit (a contiguous run of rows in both buffers).
+ *   units     device moe_ep_unit array holding every puller's list
+ *   core_off  device int32 [n_pullers, cores + 1]: puller i's core c runs
+ *             units[core_off[i, c] .. core_off[i, c + 1]) (absolute indices)
+ *   n_units   entries in `units` (bound for the core_off entries)
+ *   planes    host array of n_planes (1 or 2) plane descriptions
+ *   error_word device int32: MOE_DEVERR_UNIT is OR-ed in for every unit that
+ *             would reach outside a buffer or names a peer >= R; such a unit
+ *             is skipped (no access made)
+ * The launch waits (griddepcontrol.wait) for the kernel before it on
+ * `stream` before reading anything.  Every source row must have been written
+ * before: on one GPU, earlier in stream order; across GPUs, the caller
+ * orders the peers' writes before this call.  n_pullers = 1 is a rank of a
+ * real group; n_pullers = R pulls for a whole group emulated on one GPU
+ * (every pointer local).
+ */
+MOE_API int moe_ep_pull(const moe_ep_unit* units, const int32_t* core_off, int32_t n_units, int32_t R,
+                        int32_t cores, int32_t first_puller, int32_t n_pullers, const moe_ep_plane* planes,
+                        int32_t n_planes, int32_t* error_word, void* stream);
+
+/*
+ * Dequantize rows (the identity-expert stand-in on any buffer, e.g. a
+ * receive buffer): out[r, i] = bf16(codes[r, i] * scales[r, i / 128]) for
+ * r < rows (CloudMatrix384 write-up, "FusedDispatch and FusedCombine": INT8
+ * codes with their scale factor).
+ *   codes  device int8 [rows, H]; scales device fp32 [rows, scale_stride]
+ *   out    device bf16 [rows, H]; H a multiple of 128, scale_stride >= H/128
+ *          and a multiple of 4
+ */
+MOE_API int moe_dequant_rows(const int8_t* codes, const float* scales, int32_t rows, int32_t H,
+                             int32_t scale_stride, uint16_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_EP_H */

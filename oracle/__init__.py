@@ -257,13 +257,18 @@ def _planes(arrs):
     return arrs, ptrs
 
 
+def _row_bytes(a):
+    """Bytes per row from the shape (an empty array's strides may be 0)."""
+    return int(a.dtype.itemsize * int(np.prod(a.shape[1:], dtype=np.int64)))
+
+
 def ep_gather(pools, counts, d):
     """Dispatch exchange of one plane: pools[s] is rank s's plane [rows, ...]
     (expert-major windows); returns rank d's receive plane."""
     counts = _c(counts, np.int32)
     R, P = counts.shape
     arrs, ptrs = _planes(pools)
-    row_bytes = arrs[0].strides[0]
+    row_bytes = _row_bytes(arrs[0])
     off, _ = ep_layout(counts, d)
     out = np.zeros((int(off[-1]),) + arrs[0].shape[1:], arrs[0].dtype)
     _check(_load().orc_ep_gather(ptrs, row_bytes, _p(counts), R, P, int(d), _p(out)))
@@ -276,7 +281,7 @@ def ep_return(recvs, counts, s, rows):
     counts = _c(counts, np.int32)
     R, P = counts.shape
     arrs, ptrs = _planes(recvs)
-    row_bytes = arrs[0].strides[0]
+    row_bytes = _row_bytes(arrs[0])
     out = np.zeros((rows,) + arrs[0].shape[1:], arrs[0].dtype)
     _check(_load().orc_ep_return(ptrs, row_bytes, _p(counts), R, P, int(s), _p(out)))
     return out

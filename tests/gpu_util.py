@@ -56,6 +56,9 @@ def assert_gates_close(g_gpu, g_ref, what=""):
 def assert_y_close(y_gpu, y_ref, what=""):
     """Combine output within 1 bf16 ulp (identical unless a gate differed)."""
     d = ulp_dist_bf16(y_gpu, y_ref)
+    assert d.shape == np.shape(y_ref), f"{what}: shape {d.shape} against {np.shape(y_ref)}"
+    if d.size == 0:  # an empty batch
+        return 0
     assert d.max() <= 1, f"{what}: y differs by {d.max()} bf16 ulp"
     return int((d > 0).sum())
 

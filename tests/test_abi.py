@@ -20,9 +20,14 @@ def _desc(T=64, H=256, E=8, P=8, k=2, group=128, n_sets=2):
     return moe.Desc(T, H, E, P, k, group, n_sets)
 
 
+def _api_names():
+    from combine_moe_plan_gb300 import ep
+    return moe.header_functions() + moe.header_functions(ep.HEADER)
+
+
 def test_exports_every_header_symbol(L):
-    names = moe.header_functions()
-    assert len(names) >= 14
+    names = _api_names()
+    assert len(names) >= 20
     for n in names:
         assert hasattr(L, n), n
     # and nothing but the API is exported under the moe_ prefix
@@ -42,7 +47,7 @@ def test_trace_build_exports_probe_api(L):
     assert trace_names == ["moe_trace_reset", "moe_trace_read"]
     out = subprocess.run(["nm", "-D", "--defined-only", b.TRACE_LIB], capture_output=True, text=True).stdout
     exported = {ln.split()[-1] for ln in out.splitlines() if " T moe_" in ln}
-    assert exported == set(moe.header_functions()) | set(trace_names)
+    assert exported == set(_api_names()) | set(trace_names)
 
 
 def test_status_strings(L):

@@ -1,0 +1,166 @@
+"""The expert-parallel split on one GPU, R ranks emulated as R pools and R
+receive buffers, against the oracle's split (oracle.ep_forward), through the
+C ABI.
+
+Bar: receive buffers (INT8 codes, fp32 scales) and returned expert rows
+bit-exact, y within 1 bf16 ulp (identical in practice: the split only moves
+rows), device error word clear.  Every pull runs as one launch over all R
+pullers, so no rank's kernel waits on another's.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_plan_gb300 import ep, moe
+from combine_moe_plan_gb300 import workloads as wl
+from tests.gpu_util import assert_y_close, dev, dev_bf16, ensure_built, f32_bits, host_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _inputs(w, R, Ts=None, seed0=0):
+    Ts = Ts or [w.T] * R
+    out = []
+    for r in range(R):
+        wr = wl.dataclasses.replace(w, T=Ts[r])
+        out.append(wl.make_inputs(wr, seed=seed0 + r, with_expert_out=False))
+    return out
+
+
+def _check(g, inps, w, recv_rows, ys, counts, ref=None, recv_ex_out=None):
+    R = g.R
+    rep_off, rep_ids = inps[0]["rep_off"], inps[0]["rep_ids"]
+    if ref is None:
+        ref = oracle.ep_forward([i["logits"] for i in inps], [i["x"] for i in inps], w.k, w.P, rep_off, rep_ids,
+                                recv_ex_out=recv_ex_out)
+    np.testing.assert_array_equal(counts, ref["counts"])
+    for d in range(R):
+        n = recv_rows[d]
+        assert n == ref["recv_codes"][d].shape[0]
+        np.testing.assert_array_equal(g.recv_codes[d][:n].cpu().numpy(), ref["recv_codes"][d], err_msg=f"codes {d}")
+        np.testing.assert_array_equal(f32_bits(g.recv_scales[d][:n, :w.G].cpu().numpy()),
+                                      f32_bits(ref["recv_scales"][d]), err_msg=f"scales {d}")
+    for s in range(R):
+        rows = int(counts[s].sum())
+        np.testing.assert_array_equal(host_u16(g.views[s]["ex_out"][:rows]), ref["ex_out"][s], err_msg=f"ex_out {s}")
+        assert_y_close(host_u16(ys[s]), ref["y"][s], f"y of rank {s}")
+    assert g.check() == 0
+
+
+def _group(w, R, **kw):
+    return ep.EmulatedGroup(R, max(w.T, 1), w.H, w.E, w.P, w.k, **kw)
+
+
+def _run(g, inps, recv_ex_out=None):
+    logits = [dev(i["logits"]) for i in inps]
+    xs = [dev_bf16(i["x"]) for i in inps]
+    ro = None if inps[0]["rep_off"] is None else dev(inps[0]["rep_off"])
+    ri = None if inps[0]["rep_ids"] is None else dev(inps[0]["rep_ids"])
+    rex = None if recv_ex_out is None else [dev_bf16(a) for a in recv_ex_out]
+    ys, counts, recv_rows = g.step(logits, xs, ro, ri, recv_ex_out=rex)
+    torch.cuda.synchronize()
+    return ys, counts, recv_rows
+
+
+@pytest.mark.parametrize("R,T,cores,cap,S", [(1, 96, 4, (8, 8), (64, 64)), (2, 150, 3, (1, 1), (5, 7)),
+                                             (3, 77, 8, (2, 1), (16, 3)), (4, 64, 16, (8, 8), (1, 1))])
+def test_split_small_identity_experts(R, T, cores, cap, S):
+    """The bench workload's experts (288 physical, 32 replicas) at small
+    batches: many small units, caps that bind, single-row units."""
+    w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T), H=1024)
+    inps = _inputs(w, R)
+    g = _group(w, R, cores=cores, desc_kw=dict(fanout_cap=cap, unit_rows=S))
+    ys, counts, recv_rows = _run(g, inps)
+    _check(g, inps, w, recv_rows, ys, counts)
+
+
+def test_split_generated_expert_rows_and_ragged_batches():
+    """Receivers' expert outputs are seeded bf16 rows; the ranks' batches
+    differ in size, one rank's batch is empty."""
+    w = wl.dataclasses.replace(wl.WORKLOADS["t16384_h2048_e64_k6"], T=300)
+    R = 4
+    Ts = [300, 0, 123, 31]
+    inps = _inputs(w, R, Ts)
+    ref0 = oracle.ep_forward([i["logits"] for i in inps], [i["x"] for i in inps], w.k, w.P)
+    rng = np.random.default_rng(5)
+    rex = [wl.f32_to_bf16_bits(rng.standard_normal((c.shape[0], w.H)).astype(np.float32))
+           for c in ref0["recv_codes"]]
+    g = ep.EmulatedGroup(R, 300, w.H, w.E, w.P, w.k, cores=6)
+    ys, counts, recv_rows = _run(g, inps, rex)
+    _check(g, inps, w, recv_rows, ys, counts, recv_ex_out=rex)
+
+
+def test_split_more_ranks_than_experts_and_one_hot_expert():
+    """Six ranks over four experts (two ranks own none), and every token of
+    every rank routed to the same top-2 experts (one window holds all rows)."""
+    w = wl.Workload("tiny", T=40, H=256, E=4, P=4, k=2)
+    R = 6
+    inps = _inputs(w, R)
+    for i in inps:
+        i["logits"][:, :] = -5.0
+        i["logits"][:, 1] = 4.0
+        i["logits"][:, 2] = 3.0
+    g = _group(w, R, cores=3)
+    ys, counts, recv_rows = _run(g, inps)
+    assert sorted(recv_rows) == [0, 0, 0, 0, R * w.T, R * w.T]
+    _check(g, inps, w, recv_rows, ys, counts)
+
+
+def test_split_full_bench_shape_eight_ranks():
+    """Eight ranks of the bench workload (4096 tokens x 7168, 256 experts + 32
+    replicas, top-8) with the default group cost model: every receive buffer,
+    every returned row and every y compared in full."""
+    w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
+    R = 8
+    inps = _inputs(w, R)
+    g = _group(w, R)
+    ys, counts, recv_rows = _run(g, inps)
+    _check(g, inps, w, recv_rows, ys, counts)
+
+
+def test_one_puller_per_launch_equals_all_pullers():
+    """A rank of a real group pulls only its own lists (first_puller = its
+    rank, n_pullers = 1): R such launches build the same receive buffers."""
+    w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 200), H=512)
+    R = 3
+    inps = _inputs(w, R)
+    g = _group(w, R, cores=5)
+    _, _, recv_rows = _run(g, inps)
+    want = [g.recv_codes[d][:recv_rows[d]].clone() for d in range(R)]
+    counts = g.counts()
+    for d in range(R):
+        g.recv_codes[d].zero_()
+        s = ep.schedule(g.desc, 0, d, counts, w.H + 4 * g.Gs)
+        u, c = g.upload(ep.pack_schedules([s]))
+        ep.pull(u, c, R, g.cores, d, 1, g.disp_planes, g.error_word)
+    torch.cuda.synchronize()
+    for d in range(R):
+        assert torch.equal(g.recv_codes[d][:recv_rows[d]], want[d])
+        assert int(g.recv_codes[d][recv_rows[d]:].abs().sum().item()) == 0  # nothing written past the rows
+    assert g.check() == 0
+
+
+def test_bad_units_are_skipped_and_reported():
+    """A unit past the end of its destination buffer, one past its source
+    buffer and one naming a peer outside the group are skipped by the
+    kernel's own bounds checks and reported in the error word; the valid unit
+    beside them still lands."""
+    R, rows, H = 2, 64, 256
+    src = [torch.arange(rows * H, dtype=torch.int32, device="cuda").to(torch.int8).view(rows, H) for _ in range(R)]
+    dst = [torch.zeros((rows, H), dtype=torch.int8, device="cuda") for _ in range(R)]
+    pl = ep.plane(src, dst, H)
+    units = np.array([(1, 0, 0, 8), (0, 0, rows - 2, 4), (1, rows - 1, 0, 2), (5, 0, 0, 1)], ep.UNIT)
+    u = torch.from_numpy(units.view(np.int32).reshape(-1, 4).copy()).cuda()
+    core_off = torch.tensor([[0, 4], [4, 4]], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.pull(u, core_off, R, 1, 0, R, [pl], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == ep.DEVERR_UNIT
+    assert torch.equal(dst[0][:8], src[1][:8])
+    assert int(dst[0][8:].abs().sum().item()) == 0 and int(dst[1].abs().sum().item()) == 0
