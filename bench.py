@@ -400,10 +400,46 @@ def decode_latency(dev, reps=200):
         return _percentiles_us(ts)
 
     pct = {"dispatch": med(g_disp.replay), "combine": med(g_comb.replay), "layer": med(g_layer.replay)}
+
+    def queued(fn, n=100):
+        """GPU time of one replay whose launch the host has already queued: a
+        20 us spin kernel holds the stream while e0, the graph and e1 are
+        enqueued, so the interval excludes the host's launch latency."""
+        ts = []
+        for _ in range(n):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(40000)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return _percentiles_us(ts)
+
+    def back_to_back(fn, n=200):
+        """Mean GPU time per replay over n replays queued back to back."""
+        for _ in range(3):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    layer_q = queued(g_layer.replay)
     out = {"workload": w.name, "dispatch_us": pct["dispatch"][1], "combine_us": pct["combine"][1],
            "layer_us": pct["layer"][1], "p10_p50_p90_us": pct,
+           "layer_queued_us": layer_q[1], "layer_queued_p10_p50_p90_us": layer_q,
+           "layer_back_to_back_us": back_to_back(g_layer.replay),
            "note": "CUDA-graph replays from an idle GPU; dispatch = plan + dispatch (the fused "
-                   "dispatch carries the routing metadata); each graph launch adds its own overhead"}
+                   "dispatch carries the routing metadata); each graph launch adds its own overhead. "
+                   "layer_queued: the same layer graph with its launch already queued behind a spin "
+                   "kernel (the host's launch latency excluded); layer_back_to_back: mean per replay "
+                   "of 200 replays queued back to back (consecutive layers)"}
     if pool.check() != 0:
         raise RuntimeError("device error word set in the decode-latency pass")
     return out

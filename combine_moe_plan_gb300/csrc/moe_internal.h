@@ -12,6 +12,30 @@ namespace moe {
 
 constexpr int kGroup = 128;       // quantization group (elements)
 constexpr int kTileTokens = 32;   // tokens per placement tile (one mask word)
+constexpr int kMidTileTokens = 16;      // tile of the three-launch plan for mid-size batches
+constexpr int kMidTileMaxTokens = 2048; // largest batch that takes it
+
+// Lanes per token in the three-launch route kernel: the fewest of 8, 16, 32
+// that keep at most 8 keys a lane and leave a lane per (token, j) for the
+// gates.
+inline int route_lanes(int E, int k) {
+    const int kp = k <= 1 ? 1 : 1 << (32 - __builtin_clz((unsigned)(k - 1)));
+    return (E <= 64 && kp <= 8) ? 8 : (E <= 128 && kp <= 16) ? 16 : 32;
+}
+
+// Tokens per tile of the three-launch plan: 16 for batches of 513 to 2048
+// tokens whose tokens take a whole warp (512-thread CTAs, so that fewer
+// warps route at once on an SM), else 32.  Batches of up to 512 tokens take
+// it only when the cluster plan is refused.
+inline int route_tile_tokens(int T, int E, int k) {
+    return (T > 512 && T <= kMidTileMaxTokens && route_lanes(E, k) == 32) ? kMidTileTokens : kTileTokens;
+}
+
+// Tile-count scratch of a plan of T tokens: ceil(T / tile tokens) columns.
+inline int route_tiles(int T, int E, int k) {
+    const int tt = route_tile_tokens(T, E, k);
+    return (T + tt - 1) / tt;
+}
 constexpr int kMaxSets = 4;
 
 // Byte offsets (from the workspace base) of one buffer set's regions.
@@ -27,7 +51,7 @@ struct Geometry {
     int64_t rows;        // T_max * k
     int32_t G;           // H / 128
     int32_t Gs;          // G rounded up to a multiple of 4 (16-byte scale rows)
-    int32_t tiles_max;   // ceil(T_max / kTileTokens)
+    int32_t tiles_max;   // the most tile columns any T <= T_max uses (route_tiles)
     size_t error_word;   // offset of the shared device error word
     size_t ticket;       // offset of n_sets int32 plan tickets (single-launch plan)
     size_t control_bytes;// error word + tickets, zeroed by moe_pool_clear_error

@@ -62,7 +62,7 @@ namespace {
 // pipelined step is about 2.5 us shorter at 4096 tokens and the plan alone no
 // slower.  Smaller CTAs (8 or 16 lanes a token, for small expert counts) take
 // a quarter or half of that register file.
-template <int EPL, int THREADS>
+template <int EPL, int THREADS, int TT>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS)
 route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
                   const int32_t* __restrict__ rep_off, const int32_t* __restrict__ rep_ids,
@@ -73,8 +73,8 @@ route_tile_kernel(const float* __restrict__ logits, int T, int E, int P, int k,
     grid_dependency_sync();
     allow_dependents();
     MOE_TRACE_SM(tr_route);
-    route_tile<EPL, kRouteInRoute, THREADS>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
-                                            tile_hist, n_tiles, local_rank, err, smem, blockIdx.x);
+    route_tile<EPL, kRouteInRoute, THREADS, TT>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
+                                                tile_hist, n_tiles, local_rank, err, smem, blockIdx.x);
 }
 
 // One warp: exclusive scan of tile_hist[p, :] in place, counts[p] = column
@@ -160,7 +160,7 @@ __device__ void block_offsets(const int32_t* __restrict__ counts, int P, int32_t
 constexpr int kAssignThreads = 256;
 
 __global__ void __launch_bounds__(kAssignThreads)
-assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile_hist, int n_tiles,
+assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile_hist, int n_tiles, int tt,
               const int32_t* __restrict__ local_rank, const int32_t* __restrict__ counts, int T, int P,
               int k, int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
               int32_t* __restrict__ src_token, int32_t* __restrict__ src_k, int32_t* __restrict__ err) {
@@ -176,7 +176,7 @@ assign_kernel(const int32_t* __restrict__ phys, const int32_t* __restrict__ tile
     if (it < n) {
         p = phys[it];
         rank = local_rank[it];
-        if (p >= 0 && p < P) base = tile_hist[(size_t)p * n_tiles + (it / k) / kTileTokens];
+        if (p >= 0 && p < P) base = tile_hist[(size_t)p * n_tiles + (it / k) / tt];
     }
     block_offsets<kAssignThreads>(counts, P, offs);
     MOE_TRACE_MARK(tr_assign, 1);
@@ -393,16 +393,20 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
     const int tile = (int)cluster_ctarank();  // the grid is one cluster
     route_tile<EPL, kRouteInCluster, THREADS, TT>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
                                                   nullptr, (int)gridDim.x, nullptr, err, smem, tile);
-    // route_tile's shared-memory layout: exp table, sel_v, sel_e, sel_p [32k],
-    // masks [P], replica offsets [E+1] and ids [P]; then this kernel's arrays.
-    const int32_t* sel_p = reinterpret_cast<const int32_t*>(
-                               reinterpret_cast<float2*>(smem) + 2 * dword::kExpTableHalf + 1) +
-                           2 * TT * k;
+    // route_tile's shared-memory layout: exp table, sel_v (here: the gates),
+    // sel_e, sel_p [TT k], masks [P], replica offsets [E+1] and ids [P]; then
+    // this kernel's arrays.
+    const float* sel_g = reinterpret_cast<const float*>(reinterpret_cast<float2*>(smem) + 2 * dword::kExpTableHalf + 1);
+    const int32_t* sel_e = reinterpret_cast<const int32_t*>(sel_g + TT * k);
+    const int32_t* sel_p = sel_e + TT * k;
     const uint32_t* mask = reinterpret_cast<const uint32_t*>(sel_p + TT * k);
     int32_t* s_base = const_cast<int32_t*>(reinterpret_cast<const int32_t*>(mask + P)) + (E + 1) + P;  // [P]
     int32_t* offs = s_base + P;                                                                         // [P+1]
 
-    cluster_sync();  // every tile's masks are complete and visible in the cluster
+    // Every tile's masks are complete and visible in the cluster.  route_tile
+    // left its global stores (top-k ids, gates, physical ids) to the placement
+    // loop below, so this barrier's release has only shared memory to publish.
+    cluster_sync();
     MOE_TRACE_MARK(tr_single, 6);
 
     // Per physical expert: copies in earlier tiles and in all tiles.  Each
@@ -429,7 +433,10 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
         if (tile == 0) counts[p] = total;
         chunk += total;
     }
-    cluster_arrive();  // done reading the other CTAs' masks (waited for before exit)
+    // Done reading the other CTAs' masks (their values are consumed above, so
+    // the loads have completed; waited for before exit).  Nothing is published.
+    cluster_arrive_relaxed();
+    MOE_TRACE_MARK(tr_single, 7);
 
     // Exclusive scan of the totals into offs (warp scan, one barrier for the
     // warp totals, one to publish).
@@ -463,8 +470,10 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
         }
     }
     __syncthreads();
+    MOE_TRACE_MARK(tr_single, 8);
 
-    // Place this tile's copies: slot = offset + tile base + in-tile rank.
+    // Place this tile's copies: slot = offset + tile base + in-tile rank; and
+    // store the routing results route_tile kept in shared memory.
     const int n = T * k;
     for (int it = threadIdx.x; it < TT * k; it += THREADS) {
         const int itl = it / k;
@@ -472,6 +481,10 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
         const int t = tile * TT + itl;
         if (t >= T) continue;
         const int p = sel_p[it];
+        const size_t o = (size_t)t * k + j;
+        topk_e[o] = sel_e[it];
+        gates[o] = sel_g[it];
+        phys[o] = p;
         int r = -1;
         if (p >= 0 && p < P) r = offs[p] + s_base[p] + __popc(mask[p] & ((1u << itl) - 1u));
         if (r < 0 || r >= n) {
@@ -483,7 +496,7 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
         src_token[r] = t;
         src_k[r] = j;
     }
-    MOE_TRACE_MARK(tr_single, 7);
+    MOE_TRACE_MARK(tr_single, 9);
     cluster_wait();  // no CTA leaves while another may still read its masks
 }
 
@@ -550,28 +563,30 @@ cudaError_t launch_cluster_epl(int epl, A... a) {
     return launch_cluster<32, TT>(a...);
 }
 
-template <int EPL, int THREADS>
+template <int EPL, int THREADS, int TT>
 cudaError_t launch_route(const float* logits, int T, int E, int P, int k, const int32_t* rep_off,
                          const int32_t* rep_ids, int32_t* topk_e, float* gates, int32_t* phys, int32_t* tile_hist,
                          int32_t* local_rank, int32_t* err, size_t smem, int n_tiles, int urgent, cudaStream_t s) {
     cudaError_t e;
-    if ((e = smem_attr(route_tile_kernel<EPL, THREADS>, smem)) != cudaSuccess) return e;
-    return launch_pdl_at(urgent, route_tile_kernel<EPL, THREADS>, dim3(n_tiles), dim3(THREADS), smem, s, logits,
-                         T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank, err);
+    if ((e = smem_attr(route_tile_kernel<EPL, THREADS, TT>, smem)) != cudaSuccess) return e;
+    return launch_pdl_at(urgent, route_tile_kernel<EPL, THREADS, TT>, dim3(n_tiles), dim3(THREADS), smem, s,
+                         logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist, n_tiles, local_rank,
+                         err);
 }
 
-// The route kernel for `epl` keys a lane (a power of two up to 32 / 8).
-template <int THREADS, typename... A>
+// The route kernel for `epl` keys a lane (a power of two up to 32 / 8) and
+// tiles of TT tokens (L = THREADS / TT lanes a token).
+template <int THREADS, int TT = kTileTokens, typename... A>
 cudaError_t launch_route_epl(int epl, A... a) {
-    if (epl <= 1) return launch_route<1, THREADS>(a...);
-    if (epl <= 2) return launch_route<2, THREADS>(a...);
-    if (epl <= 4) return launch_route<4, THREADS>(a...);
-    if constexpr (THREADS == kRouteThreads) {
-        if (epl <= 8) return launch_route<8, THREADS>(a...);
-        if (epl <= 16) return launch_route<16, THREADS>(a...);
-        return launch_route<32, THREADS>(a...);
+    if (epl <= 1) return launch_route<1, THREADS, TT>(a...);
+    if (epl <= 2) return launch_route<2, THREADS, TT>(a...);
+    if (epl <= 4) return launch_route<4, THREADS, TT>(a...);
+    if constexpr (THREADS / TT == 32) {
+        if (epl <= 8) return launch_route<8, THREADS, TT>(a...);
+        if (epl <= 16) return launch_route<16, THREADS, TT>(a...);
+        return launch_route<32, THREADS, TT>(a...);
     } else {
-        return launch_route<8, THREADS>(a...);
+        return launch_route<8, THREADS, TT>(a...);
     }
 }
 
@@ -667,31 +682,38 @@ cudaError_t launch_plan(const float* logits, int T, int E, int P, int k, const i
         return e;
     }
 
-    // Lanes per token in the route kernel: the fewest of 8, 16, 32 that keep
-    // at most 8 keys a lane and leave a lane per (token, j) for the gates.
-    const int kp = k <= 1 ? 1 : 1 << (32 - __builtin_clz((unsigned)(k - 1)));
-    const int L = (E <= 64 && kp <= 8) ? 8 : (E <= 128 && kp <= 16) ? 16 : 32;
+    // Three launches.  Lanes per token: route_lanes; tokens per tile:
+    // route_tile_tokens (16 for mid-size batches of whole-warp tokens).  The
+    // tile-count scratch has route_tiles(T) columns.
+    const int L = route_lanes(E, k);
+    const int tt = route_tile_tokens(T, E, k);
+    const int tiles = (T + tt - 1) / tt;
+    const size_t rsmem = route_smem(tt, E, P, k);
     const int epl = (E + L - 1) / L;
     if (L == 8)
         e = launch_route_epl<256>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
-                                  local_rank, err, smem, n_tiles, urgent, s);
+                                  local_rank, err, rsmem, tiles, urgent, s);
     else if (L == 16)
         e = launch_route_epl<512>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys, tile_hist,
-                                  local_rank, err, smem, n_tiles, urgent, s);
+                                  local_rank, err, rsmem, tiles, urgent, s);
+    else if (tt == kMidTileTokens)
+        e = launch_route_epl<32 * kMidTileTokens, kMidTileTokens>(epl, logits, T, E, P, k, rep_off, rep_ids,
+                                                                   topk_e, gates, phys, tile_hist, local_rank, err,
+                                                                   rsmem, tiles, urgent, s);
     else
         e = launch_route_epl<kRouteThreads>(epl, logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
-                                            tile_hist, local_rank, err, smem, n_tiles, urgent, s);
+                                            tile_hist, local_rank, err, rsmem, tiles, urgent, s);
     if (e != cudaSuccess) return e;
     *launches += 1;
 
-    e = launch_pdl_at(urgent, column_scan_kernel, dim3((P + 7) / 8), dim3(kScanThreads), 0, s, tile_hist, n_tiles,
+    e = launch_pdl_at(urgent, column_scan_kernel, dim3((P + 7) / 8), dim3(kScanThreads), 0, s, tile_hist, tiles,
                       P, counts);
     if (e != cudaSuccess) return e;
     *launches += 1;
 
     const int n = T * k;
     e = launch_pdl_at(urgent, assign_kernel, dim3((n + kAssignThreads - 1) / kAssignThreads),
-                      dim3(kAssignThreads), (P + 1) * sizeof(int32_t), s, phys, (const int32_t*)tile_hist, n_tiles,
+                      dim3(kAssignThreads), (P + 1) * sizeof(int32_t), s, phys, (const int32_t*)tile_hist, tiles, tt,
                       (const int32_t*)local_rank, (const int32_t*)counts, T, P, k, offsets, slot, src_token,
                       src_k, err);
     if (e != cudaSuccess) return e;

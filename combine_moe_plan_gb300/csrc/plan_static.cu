@@ -127,7 +127,7 @@ extern "C" MOE_API int moe_plan_static(const float* logits, int32_t T, int32_t E
         if (!aligned16(p)) return MOE_ERR_ALIGN;
     if (rep_off != nullptr && (!aligned16(rep_off) || !aligned16(rep_ids))) return MOE_ERR_ALIGN;
 
-    const size_t n_tiles = ((size_t)T + moe::kTileTokens - 1) / moe::kTileTokens;
+    const size_t n_tiles = (size_t)moe::route_tiles(T, E, k);
     const size_t hist_bytes = round256((size_t)P * n_tiles * sizeof(int32_t));
     const size_t rank_bytes = round256((size_t)T * (size_t)k * sizeof(int32_t));
     if (hist_bytes + rank_bytes > kStaticScratchBytes) return MOE_ERR_SIZE;

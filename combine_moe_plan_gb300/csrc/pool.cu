@@ -6,6 +6,7 @@
 // buffers, sized once for the worst case, carved from one caller-owned
 // workspace, with n_sets copies so consecutive iterations alternate sets.
 // No call allocates; every launch is asynchronous on the caller's stream.
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <vector>
@@ -45,7 +46,9 @@ int make_geometry(const moe_desc* d, Geometry* g) {
     g->rows = (int64_t)d->T_max * d->k;
     g->G = d->H / kGroup;
     g->Gs = (g->G + 3) / 4 * 4;
-    g->tiles_max = (d->T_max + kTileTokens - 1) / kTileTokens;
+    // route_tiles over T <= T_max: ceil(T / 32), or ceil(T / 16) up to 2048 tokens.
+    g->tiles_max = std::max(route_tiles(d->T_max, d->E, d->k),
+                            route_tiles(std::min(d->T_max, kMidTileMaxTokens), d->E, d->k));
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;

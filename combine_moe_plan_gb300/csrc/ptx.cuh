@@ -76,6 +76,12 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // writes before the arrive are visible to every CTA after its wait.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// Arrive without memory ordering: for a thread whose remote shared-memory
+// loads have all been consumed (so they have completed) and that publishes
+// nothing to the cluster, e.g. to say "done reading your shared memory".
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_sync() {
     cluster_arrive();
     cluster_wait();

@@ -259,10 +259,12 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
             }
             if (p < 0) set_error(err, MOE_DEVERR_REPLICA);
         }
-        const size_t o = (size_t)tt * k + ij;
-        topk_e[o] = e;
-        gates[o] = g;
-        phys[o] = p;
+        if (WHERE != kRouteInCluster) {  // the cluster plan stores these after its barrier
+            const size_t o = (size_t)tt * k + ij;
+            topk_e[o] = e;
+            gates[o] = g;
+            phys[o] = p;
+        }
         sel_p[it] = p;
         if (p >= 0) {
             const uint32_t bit = 1u << itl;
@@ -272,6 +274,9 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     }
     __syncthreads();
     ROUTE_MARK(4);
+    // In the cluster plan the gate goes to shared memory (sel_v is not read
+    // after the barrier above) for the stores after the cluster barrier.
+    if (WHERE == kRouteInCluster && item_ok) sel_v[it] = g;
 
     // ---- tile histogram (expert-major) and in-tile ranks ----
     if (WHERE != kRouteInCluster) {

@@ -14,7 +14,7 @@
 namespace moe {
 
 constexpr int kTraceCtas = 8192;  // CTAs recorded per kernel (later CTAs are not)
-constexpr int kTraceStages = 8;   // stage stamps per CTA
+constexpr int kTraceStages = 12;  // stage stamps per CTA
 
 // Trace slots: one per kernel kind.
 enum TraceKind : int {

@@ -24,15 +24,16 @@ import numpy as np
 from combine_moe_plan_gb300 import build as moe_build
 from combine_moe_plan_gb300 import moe
 
-TRACE_CTAS, TRACE_STAGES = 8192, 8
+TRACE_CTAS, TRACE_STAGES = 8192, 12
 KINDS = {
     0: ("route_tile", ["start", "top-k", "gates(pairs)", "fallback", "replicas+masks", "counts+ranks"]),
     1: ("column_scan", ["start", "end"]),
     2: ("assign", ["start", "offsets", "end"]),
-    # one plan launch: the cluster kernel (stage 6 = cluster barrier passed) or,
-    # without clusters, the ticket kernel (stage 6 = its last CTA's scans done)
+    # one plan launch: the cluster kernel (6 cluster barrier passed, 7 the other
+    # tiles' masks read, 8 offsets scanned, 9 copies placed) or, without
+    # clusters, the ticket kernel (6 its last CTA's tail start, 7 end)
     3: ("plan_one_launch", ["start", "top-k", "gates(pairs)", "fallback", "replicas+masks", "counts+ranks",
-                            "barrier|scans", "end"]),
+                            "barrier|tail", "masks read|end", "offsets", "placed"]),
     4: ("dispatch", ["start", "quantized", "slots", "stored"]),
     5: ("combine", ["start", "slots", "accumulated", "stored"]),
 }
@@ -85,7 +86,20 @@ def summarize(kind: int, n_ctas: int) -> dict:
     if started.size:
         out["span_ns"] = float(last.max() - started.min())
         out["cta_ns_median"] = float(np.median(last[ns[:, 0] > 0] - started))
+        out["first_start_ns"] = int(started.min())  # %globaltimer, common to all SMs
+        out["last_end_ns"] = int(last.max())
     return out
+
+
+def timeline(rows: list) -> list:
+    """First start and last end of each launch in ns after the first launch's
+    start (the gaps between consecutive kernels of one pass)."""
+    t0 = min(r["first_start_ns"] for r in rows if "first_start_ns" in r)
+    for r in rows:
+        if "first_start_ns" in r:
+            r["start_at_ns"] = r.pop("first_start_ns") - t0
+            r["end_at_ns"] = r.pop("last_end_ns") - t0
+    return rows
 
 
 def run(workload: str, seed: int = 0) -> list:
@@ -107,7 +121,7 @@ def run(workload: str, seed: int = 0) -> list:
     for _ in range(3):  # warm: the last pass is the one read back
         reset()
         pool.plan(logits, ro, ri)
-        pool.dispatch(x)
+        pool.dispatch(x, after_plan=True)
         pool.combine(w.T, y=y)
     torch.cuda.synchronize()
     if pool.check() != 0:
@@ -121,7 +135,7 @@ def run(workload: str, seed: int = 0) -> list:
         rows += [summarize(0, n_tiles), summarize(1, (w.P + 7) // 8), summarize(2, (w.rows + 255) // 256)]
     rows.append(summarize(4, min(TRACE_CTAS, (w.T * ((w.H + 511) // 512) + 7) // 8)))
     rows.append(summarize(5, min(TRACE_CTAS, (w.T * ((w.H + 255) // 256) + 7) // 8)))
-    return rows
+    return timeline(rows)
 
 
 def main(argv=None):

@@ -201,7 +201,8 @@ MOE_API int moe_replica_check(const int32_t* rep_off, const int32_t* rep_ids, in
  * src_token, src_k of the set.  0 <= T <= T_max; T = 0 (an empty batch)
  * zeroes counts and offsets and launches no kernel (logits may be NULL).
  * Kernels: up to 512 tokens one thread-block cluster; beyond, three
- * launches (route, column scan, assign).  With the environment variable
+ * launches (route, column scan, assign), routing tiles of 16 tokens up to
+ * 2048 tokens when E > 128 or k > 16, else 32.  With the environment variable
  * MOE_PLAN_NO_CLUSTER=1 (read once per process), or on a device that refuses
  * the cluster, batches of up to 128 tokens take one launch whose last CTA
  * finishes the placement, and larger ones the three launches.  The results
@@ -288,9 +289,10 @@ MOE_API int moe_step_host(moe_pool* pool, const float* h_logits, const uint16_t*
  * Its scratch (per-tile expert counts and in-tile ranks) lives in a fixed
  * 4 MiB array in this library's device image, held on every GPU that loads it
  * until the process exits.  Sizes whose scratch needs more,
- * 4 * (P * ceil(T / 32) + T * k) bytes (each part rounded up to 256), return
- * MOE_ERR_SIZE before anything is launched.  No cudaMalloc or cudaFree is
- * called.
+ * 4 * (P * ceil(T / TT) + T * k) bytes (each part rounded up to 256), return
+ * MOE_ERR_SIZE before anything is launched; TT, the plan's tile, is 16 tokens
+ * for batches of 513 to 2048 tokens with E > 128 or k > 16, else 32.  No
+ * cudaMalloc or cudaFree is called.
  *   - All calls share that array: calls whose kernels overlap on the GPU
  *     (other streams, other host threads) race and give wrong slots.  Batches
  *     of up to 512 tokens take the cluster plan, which keeps its scratch in

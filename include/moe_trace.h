@@ -28,15 +28,16 @@ extern "C" {
 #endif
 
 #define MOE_TRACE_CTAS 8192
-#define MOE_TRACE_STAGES 8
+#define MOE_TRACE_STAGES 12
 
 typedef enum moe_trace_kind {
     MOE_TRACE_ROUTE = 0,       /* route_tile: 0 start, 1 top-k, 2 exp, 3 sums, 4 gates+masks, 5 counts+ranks */
     MOE_TRACE_COLUMN_SCAN = 1, /* column_scan: 0 start, 1 end */
     MOE_TRACE_ASSIGN = 2,      /* assign: 0 start, 1 offsets, 2 end */
     MOE_TRACE_PLAN_SINGLE = 3, /* one-launch plan, 0-5 as route: the cluster kernel (6 cluster
-                                  barrier passed, 7 copies placed) or, without clusters, the
-                                  ticket kernel (last CTA: 6 tail start, 7 end) */
+                                  barrier passed, 7 other tiles' masks read, 8 offsets
+                                  scanned, 9 copies placed) or, without clusters, the ticket
+                                  kernel (last CTA: 6 tail start, 7 end) */
     MOE_TRACE_DISPATCH = 4,    /* dispatch (warp 0): 0 start, 1 quantized, 2 slots read, 3 stored */
     MOE_TRACE_COMBINE = 5,     /* combine (warp 0): 0 start, 1 slots, 2 accumulated, 3 stored */
     MOE_TRACE_KINDS = 6

@@ -460,6 +460,25 @@ def test_plan_path_switch_at_cluster_sizes():
                 seed=int(rng.integers(1 << 30)), T_max=513, pool=pool)
 
 
+def test_plan_mid_size_tiles():
+    """513 to 2048 tokens whose tokens take a whole warp route in 16-token
+    tiles (512-thread CTAs); beyond 2048, 32-token tiles again.  Every switch
+    point and a ragged tail of each tile size on one pool sized for 3000
+    tokens, one after the other in both orders; then a pool sized for 700
+    tokens, whose tile-count scratch holds ceil(700 / 16) columns."""
+    rng = np.random.default_rng(14)
+    E, P, k, H = 256, 288, 8, 256
+    inp = wl.make_inputs(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 3000))
+    pool = moe.Pool(3000, H, E, P, k, n_sets=2)
+    for T in (513, 527, 528, 1000, 2047, 2048, 2049, 3000, 2048, 1025, 512, 513):
+        _custom(T, H, E, P, k, inp["logits"][:T], rep_off=inp["rep_off"], rep_ids=inp["rep_ids"],
+                seed=int(rng.integers(1 << 30)), T_max=3000, pool=pool)
+    pool = moe.Pool(700, H, E, P, k, n_sets=1)
+    for T in (700, 513, 699):
+        _custom(T, H, E, P, k, inp["logits"][:T], rep_off=inp["rep_off"], rep_ids=inp["rep_ids"],
+                seed=int(rng.integers(1 << 30)), T_max=700, pool=pool)
+
+
 def test_three_launch_plan_at_maximum_shapes():
     """More than 32 tiles (so the route / column-scan / assign kernels run)
     at the largest shapes the API takes: E = 1024, P = 4096 (four replicas per

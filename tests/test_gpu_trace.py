@@ -30,3 +30,8 @@ def test_trace_stages(workload):
         # every CTA of the launch was stamped at its first and last stage
         first = next(iter(x["stages"].values()))
         assert first["ctas"] == x["ctas"] or x["kernel"] in ("plan_one_launch",)
+        assert 0 <= x["start_at_ns"] < x["end_at_ns"]
+    # one pass: each kernel ends after the one before it (PDL lets a kernel
+    # start early, but it finishes only after its predecessor's results)
+    ends = [x["end_at_ns"] for x in rows]
+    assert ends == sorted(ends)

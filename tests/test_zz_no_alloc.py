@@ -47,7 +47,7 @@ def _compare(got, ref, what):
 def test_plan_static_matches_plan_two_calls_in_a_row():
     ensure_built()
     cases = [wl.WORKLOADS["t4096_h7168_e256p288_k8"], wl.small_variant(wl.WORKLOADS["t16384_h2048_e64_k6"], 3000),
-             wl.WORKLOADS["t96_h7168_e256_k8"]]
+             wl.WORKLOADS["t96_h7168_e256_k8"], wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 1500)]
     refs, gots = [], []
     for w in cases:
         inp = wl.make_inputs(w, with_expert_out=False)
