@@ -66,6 +66,9 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
     ap.add_argument("--ep-ranks", type=int, default=8,
                     help="ranks of the expert-parallel split emulated on this GPU (0: skip that phase)")
+    ap.add_argument("--ep-only", action="store_true",
+                    help="run only the emulated split (profiling: with --ep-tokens, a case of a few GB)")
+    ap.add_argument("--ep-tokens", type=int, default=0, help="tokens per rank of the split (0: the workload's)")
     return ap.parse_args()
 
 
@@ -431,15 +434,26 @@ def decode_latency(dev, reps=200):
         return e0.elapsed_time(e1) * 1e3 / n
 
     layer_q = queued(g_layer.replay)
+    # The floor of a graph of three kernels that do nothing (torch adds on 16
+    # floats), queued the same way: what any three-kernel graph costs.
+    tiny = torch.zeros(16, device=dev)
+    g_empty = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_empty, stream=s):
+        for _ in range(3):
+            tiny.add_(1.0)
+    torch.cuda.synchronize()
+    empty_q = queued(g_empty.replay)
     out = {"workload": w.name, "dispatch_us": pct["dispatch"][1], "combine_us": pct["combine"][1],
            "layer_us": pct["layer"][1], "p10_p50_p90_us": pct,
            "layer_queued_us": layer_q[1], "layer_queued_p10_p50_p90_us": layer_q,
            "layer_back_to_back_us": back_to_back(g_layer.replay),
+           "empty_three_kernel_graph_queued_us": empty_q[1],
            "note": "CUDA-graph replays from an idle GPU; dispatch = plan + dispatch (the fused "
                    "dispatch carries the routing metadata); each graph launch adds its own overhead. "
                    "layer_queued: the same layer graph with its launch already queued behind a spin "
                    "kernel (the host's launch latency excluded); layer_back_to_back: mean per replay "
-                   "of 200 replays queued back to back (consecutive layers)"}
+                   "of 200 replays queued back to back (consecutive layers); empty_three_kernel_graph: "
+                   "a graph of three do-nothing kernels queued the same way (the graph's own cost)"}
     if pool.check() != 0:
         raise RuntimeError("device error word set in the decode-latency pass")
     return out
@@ -800,11 +814,27 @@ def _e2e(a, w, inp, rep_off, rep_ids, dev, ws):
     return e2e_ms
 
 
+def run_ep_only(a, w):
+    """Only the emulated split, printed as one JSON line (a profiling aid)."""
+    import torch
+    from combine_moe_plan_gb300 import build as moe_build
+    from combine_moe_plan_gb300 import moe
+    moe_build.build()
+    moe.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if a.ep_tokens:
+        w = wl.small_variant(w, a.ep_tokens)
+    print(json.dumps({"ep_split_emulated": ep_split(dev, w, a.ep_ranks, reps=a.steps)}), flush=True)
+
+
 def main():
     a = _args()
     w = wl.WORKLOADS[a.workload]
     if a.impl == "reference":
         run_reference(a, w)
+    elif a.ep_only:
+        run_ep_only(a, w)
     else:
         run_ours(a, w)
 

@@ -102,8 +102,12 @@ def timeline(rows: list) -> list:
     return rows
 
 
-def run(workload: str, seed: int = 0) -> list:
-    """One plan + dispatch + combine of `workload` under the trace build."""
+def run(workload: str, seed: int = 0, graph: bool = False, reps: int = 20) -> list:
+    """One plan + dispatch + combine of `workload` under the trace build.
+    With graph=True the three calls are captured as one CUDA graph and
+    replayed `reps` times, each replay queued behind a spin kernel (so that
+    it runs as it would inside a longer decode step); the stamps of every
+    replay are read back and the median of each figure is reported."""
     import torch
     from combine_moe_plan_gb300 import workloads as wl
     load()
@@ -118,15 +122,56 @@ def run(workload: str, seed: int = 0) -> list:
     if "ex_out" in inp:
         pool.view(0)["ex_out"][: w.rows].copy_(torch.from_numpy(inp["ex_out"].view(np.int16)).view(torch.bfloat16))
     y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
-    for _ in range(3):  # warm: the last pass is the one read back
-        reset()
-        pool.plan(logits, ro, ri)
-        pool.dispatch(x, after_plan=True)
-        pool.combine(w.T, y=y)
+    s = torch.cuda.Stream(device=dev)
+
+    def layer():
+        pool.plan(logits, ro, ri, stream=s)
+        pool.dispatch(x, after_plan=True, stream=s)
+        pool.combine(w.T, y=y, stream=s)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):  # warm: the last pass is the one read back
+            reset(s)
+            layer()
     torch.cuda.synchronize()
     if pool.check() != 0:
         raise RuntimeError("device error word set")
-    n_tiles = (w.T + 31) // 32
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            layer()
+        torch.cuda.synchronize()
+        passes = []
+        for _ in range(reps):
+            reset()
+            torch.cuda.synchronize()
+            torch.cuda._sleep(40000)
+            g.replay()
+            torch.cuda.synchronize()
+            passes.append(_pass_rows(w))
+        return _median_rows(passes)
+    return _pass_rows(w)
+
+
+def _median_rows(passes: list) -> list:
+    """Per kernel, the median over passes of every numeric figure."""
+    out = []
+    for rows in zip(*passes):
+        r = dict(rows[0])
+        for key in ("span_ns", "cta_ns_median", "start_at_ns", "end_at_ns"):
+            if key in r:
+                r[key] = float(np.median([x[key] for x in rows]))
+        r["stages"] = {st: {"median_ns": float(np.median([x["stages"][st]["median_ns"] for x in rows
+                                                          if st in x["stages"]])),
+                            "ctas": r["stages"][st]["ctas"]} for st in r["stages"]}
+        r["passes"] = len(rows)
+        out.append(r)
+    return out
+
+
+def _pass_rows(w) -> list:
+    """The stamps of the last pass, per kernel, on a common time axis."""
+    n_tiles = (w.T + 15) // 16  # enough for either tile size: unused CTA slots are zero and skipped
     rows = []
     one = summarize(3, 32)  # one plan launch: the cluster kernel, or the ticket kernel without clusters
     if one["ctas"] > 0:
@@ -141,8 +186,9 @@ def run(workload: str, seed: int = 0) -> list:
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="t96_h7168_e256_k8")
+    ap.add_argument("--graph", action="store_true", help="replay the three calls as one CUDA graph")
     a = ap.parse_args(argv)
-    for r in run(a.workload):
+    for r in run(a.workload, graph=a.graph):
         print(json.dumps(r))
 
 

@@ -12,10 +12,11 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.mark.parametrize("workload", ["t96_h7168_e256_k8", "t4096_h7168_e256p288_k8"])
-def test_trace_stages(workload):
-    r = subprocess.run([sys.executable, "-m", "combine_moe_plan_gb300.trace", "--workload", workload],
-                       capture_output=True, text=True, cwd=ROOT, timeout=600)
+@pytest.mark.parametrize("workload,graph", [("t96_h7168_e256_k8", False), ("t4096_h7168_e256p288_k8", False),
+                                            ("t96_h7168_e256_k8", True)])
+def test_trace_stages(workload, graph):
+    r = subprocess.run([sys.executable, "-m", "combine_moe_plan_gb300.trace", "--workload", workload] +
+                       (["--graph"] if graph else []), capture_output=True, text=True, cwd=ROOT, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     rows = [json.loads(ln) for ln in r.stdout.splitlines() if ln.startswith("{")]
     names = [x["kernel"] for x in rows]
