@@ -276,12 +276,15 @@ def test_launch_count():
     _check_all(big, inp, Run(big, inp, pool=pool))
 
 
+@pytest.mark.parametrize("after_plan", [False, True])
 @pytest.mark.parametrize("T", [40, 96, 200, 512, 1000])
-def test_step_captures_in_a_cuda_graph(T):
+def test_step_captures_in_a_cuda_graph(T, after_plan):
     """plan -> dispatch -> combine (PDL launches) captured once in a CUDA graph
     and replayed on new input contents gives the oracle's results: 40, 96, 200
     and 512 tokens (cluster plans of 5 CTAs of 8 tokens, 6 of 16, 7 of 32 and
-    16 of 32) and 1000 (the three launches)."""
+    16 of 32) and 1000 (the three launches).  With after_plan the dispatch
+    waits on the cluster plan's per-tile flags, which every replay's plan
+    clears and sets again."""
     w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T)
     pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
     inp0 = wl.make_inputs(w, seed=0)
@@ -291,15 +294,15 @@ def test_step_captures_in_a_cuda_graph(T):
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):  # warm
         pool.plan(logits, ro, ri, buf=1, stream=s)
-        pool.dispatch(x, buf=1, stream=s)
+        pool.dispatch(x, buf=1, stream=s, after_plan=after_plan)
         pool.combine(w.T, y=y, ex_out=ex, buf=1, stream=s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         pool.plan(logits, ro, ri, buf=1, stream=s)
-        pool.dispatch(x, buf=1, stream=s)
+        pool.dispatch(x, buf=1, stream=s, after_plan=after_plan)
         pool.combine(w.T, y=y, ex_out=ex, buf=1, stream=s)
-    for seed in (3, 4):
+    for seed in (3, 4, 5):
         inp = wl.make_inputs(w, seed=seed)
         logits.copy_(dev(inp["logits"]))
         x.copy_(dev_bf16(inp["x"]))
@@ -503,7 +506,8 @@ def test_cluster_plan_at_maximum_shapes(T):
     _custom(T, 128, E, P, 32, rng.standard_normal((T, E)), rep_off=off, rep_ids=ids, seed=T)
 
 
-def test_bench_schedule_two_streams_full_size():
+@pytest.mark.parametrize("after_plan", [False, True])
+def test_bench_schedule_two_streams_full_size(after_plan):
     """The bench's timed schedule at the bench workload's full size: steps
     alternate the two buffer sets on two streams, launched back to back, each
     step with its own inputs and output buffer; every step's result is
@@ -525,7 +529,7 @@ def test_bench_schedule_two_streams_full_size():
     for i, (_, logits, x, ex, ro, ri, y) in enumerate(steps):
         s, b = streams[i & 1], i & 1
         pool.plan(logits, ro, ri, buf=b, stream=s)
-        pool.dispatch(x, buf=b, stream=s)
+        pool.dispatch(x, buf=b, stream=s, after_plan=after_plan)
         pool.combine(w.T, y=y, ex_out=ex, buf=b, stream=s)
     torch.cuda.synchronize()
     assert pool.check() == 0
@@ -542,15 +546,19 @@ def test_bench_schedule_two_streams_full_size():
         np.testing.assert_array_equal(v["codes"][:w.rows].cpu().numpy(), codes)
 
 
+@pytest.mark.parametrize("after_plan", [False, True])
 @pytest.mark.parametrize("name,T", [("t96_h7168_e256_k8", 96), ("t4096_h7168_e256p288_k8", 300),
                                     ("t16384_h2048_e64_k6", 1000), ("t16384_h2048_e64_k6", 2000)])
-def test_layers_chained_on_one_stream(name, T):
+def test_layers_chained_on_one_stream(name, T, after_plan):
     """Six layers back to back on one stream, each layer's y the next layer's x,
     the two buffer sets alternating, no synchronization in between; then the
     same chain captured once as a CUDA graph and replayed.  Every layer's y
-    equals the oracle run layer after layer on its own outputs.  Dispatch reads
-    x before its wait for the plan, so this checks that the previous layer's
-    combine has finished writing x by then (the plan in between waits for it).
+    equals the oracle run layer after layer on its own outputs.  With
+    after_plan, dispatch reads x before its wait for the plan (and after a
+    cluster plan waits on per-tile flags, not the plan grid), so this checks
+    that the previous layer's combine has finished writing x by then (the
+    plan in between waits for it) and that each layer's plan re-arms its
+    flags.
     The plan forms covered: cluster (96 tokens as 6 CTAs of 16, 300 as 10 of
     32) and three launches (1000 and 2000 tokens, 8-lane segments at 64
     experts); the test run without clusters adds the ticket kernel."""
@@ -576,7 +584,7 @@ def test_layers_chained_on_one_stream(name, T):
         for l in range(L):
             b = l & 1
             pool.plan(lg[l], ro[l], ri[l], buf=b, stream=s)
-            pool.dispatch(xin, buf=b, stream=s)
+            pool.dispatch(xin, buf=b, stream=s, after_plan=after_plan)
             pool.identity_experts(w.T, buf=b, stream=s)
             pool.combine(w.T, y=ys[l], buf=b, stream=s)
             xin = ys[l]
