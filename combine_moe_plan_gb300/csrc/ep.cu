@@ -19,6 +19,7 @@
 // plain memcpy; the schedule decides which core moves what, in which order.
 #include <algorithm>
 #include <cstring>
+#include <functional>
 #include <thread>
 #include <vector>
 
@@ -175,15 +176,32 @@ int check_schedule_args(const moe_ep_desc* desc, int32_t direction, const int32_
 void schedule_one(const moe_ep_desc& desc, const Windows& w, const int32_t* counts, int32_t direction,
                   int32_t puller, int64_t row_bytes, Schedule* out) {
     const int32_t R = desc.R, P = desc.P, C = desc.cores;
+    auto cost_of = [&](int t, int64_t rows) {
+        return desc.alpha_ns[t] * 1000 + rows * row_bytes * 1000 / desc.beta_gbs[t];
+    };
+    const int64_t full_cost[2] = {cost_of(0, desc.unit_rows[0]), cost_of(1, desc.unit_rows[1])};
+
+    // 1. units in ascending destination row.  A full unit (S_t rows) of tier t
+    // costs full_cost[t], so the full units of a tier are already in order
+    // among themselves; only the shorter last pieces of windows need sorting.
     std::vector<moe_ep_unit> u;
-    std::vector<int64_t> cost;
+    std::vector<int32_t> full[2];
+    struct Key {
+        int64_t cost;
+        int32_t idx;
+    };
+    std::vector<Key> tails;
     auto cut = [&](int32_t peer, int64_t src0, int64_t dst0, int64_t n) {
         const int t = peer == puller ? 0 : 1;
         const int64_t S = desc.unit_rows[t];
         for (int64_t at = 0; at < n; at += S) {
             const int64_t rows = std::min(S, n - at);
+            const int32_t idx = (int32_t)u.size();
             u.push_back(moe_ep_unit{peer, (int32_t)(src0 + at), (int32_t)(dst0 + at), (int32_t)rows});
-            cost.push_back(desc.alpha_ns[t] * 1000 + rows * row_bytes * 1000 / desc.beta_gbs[t]);
+            if (rows == S)
+                full[t].push_back(idx);
+            else
+                tails.push_back(Key{cost_of(t, rows), idx});
         }
     };
     if (direction == 0) {
@@ -196,26 +214,44 @@ void schedule_one(const moe_ep_desc& desc, const Windows& w, const int32_t* coun
                 counts[(size_t)puller * P + p]);
     }
     const int32_t nu = (int32_t)u.size();
-    struct Key {
-        int64_t cost;
-        int32_t idx;
-    };
-    std::vector<Key> order(nu);
-    for (int32_t k = 0; k < nu; ++k) order[k] = Key{cost[k], k};
-    std::sort(order.begin(), order.end(),
-              [](const Key& a, const Key& b) { return a.cost != b.cost ? a.cost > b.cost : a.idx < b.idx; });
 
-    // Cores sit in a binary heap by (load, core); a unit takes the first
+    // 2. longest first, equal costs in enumeration order: merge the two runs
+    // of full units with the sorted tails.
+    auto later = [](const Key& a, const Key& b) { return a.cost != b.cost ? a.cost < b.cost : a.idx > b.idx; };
+    std::sort(tails.begin(), tails.end(), [&](const Key& a, const Key& b) { return later(b, a); });
+    std::vector<Key> order;
+    order.reserve(nu);
+    {
+        size_t i0 = 0, i1 = 0, it = 0;
+        while (order.size() < (size_t)nu) {
+            Key best{-1, -1};
+            int from = -1;
+            if (i0 < full[0].size()) best = Key{full_cost[0], full[0][i0]}, from = 0;
+            if (i1 < full[1].size()) {
+                const Key c{full_cost[1], full[1][i1]};
+                if (from < 0 || later(best, c)) best = c, from = 1;
+            }
+            if (it < tails.size() && (from < 0 || later(best, tails[it]))) best = tails[it], from = 2;
+            order.push_back(best);
+            if (from == 0) ++i0;
+            else if (from == 1) ++i1;
+            else ++it;
+        }
+    }
+
+    // 3. list scheduling under the fan-out cap.  Cores sit in a min-heap of
+    // (load, core) packed into one 128-bit key; a unit takes the first
     // eligible core popped, i.e. the least-loaded eligible core with ties to
     // the lower core.  A core with the longest list is always eligible (its
     // next stripe is still empty), so the search ends.
-    std::vector<int64_t> load(C, 0);
+    using Slot = unsigned __int128;
+    auto slot_of = [](int64_t load, int32_t c) { return ((Slot)(uint64_t)load << 32) | (uint32_t)c; };
     std::vector<int32_t> len(C, 0), core_of(nu), pos(nu);
+    std::vector<int64_t> load(C, 0);
     std::vector<int32_t> stripe;  // stripe[i * R + q]: cores whose i-th unit is from peer q
-    auto above = [&](int32_t a, int32_t b) { return load[a] != load[b] ? load[a] > load[b] : a > b; };
-    std::vector<int32_t> heap(C), held;
-    for (int32_t c = 0; c < C; ++c) heap[c] = c;
-    std::make_heap(heap.begin(), heap.end(), above);
+    std::vector<Slot> heap(C), held;
+    for (int32_t c = 0; c < C; ++c) heap[c] = slot_of(0, c);  // already a heap: ascending
+    const std::greater<Slot> above;
     for (int32_t k = 0; k < nu; ++k) {
         const int32_t i = order[k].idx;
         const int32_t q = u[i].peer;
@@ -224,13 +260,14 @@ void schedule_one(const moe_ep_desc& desc, const Windows& w, const int32_t* coun
         int32_t best = -1;
         while (best < 0) {
             std::pop_heap(heap.begin(), heap.end(), above);
-            const int32_t c = heap.back();
+            const Slot top = heap.back();
             heap.pop_back();
+            const int32_t c = (int32_t)(uint32_t)top;
             const size_t at = (size_t)len[c] * R + q;
             if (at >= stripe.size() || stripe[at] < cap)
                 best = c;
             else
-                held.push_back(c);
+                held.push_back(top);
         }
         const size_t at = (size_t)len[best] * R + q;
         if (at >= stripe.size()) stripe.resize(((size_t)len[best] + 1) * R * 2, 0);
@@ -238,10 +275,10 @@ void schedule_one(const moe_ep_desc& desc, const Windows& w, const int32_t* coun
         core_of[i] = best;
         pos[i] = len[best];
         len[best] += 1;
-        load[best] += cost[i];
-        held.push_back(best);
-        for (int32_t c : held) {
-            heap.push_back(c);
+        load[best] += order[k].cost;
+        held.push_back(slot_of(load[best], best));
+        for (const Slot& h : held) {
+            heap.push_back(h);
             std::push_heap(heap.begin(), heap.end(), above);
         }
     }
