@@ -69,6 +69,8 @@ def _args():
     ap.add_argument("--ep-only", action="store_true",
                     help="run only the emulated split (profiling: with --ep-tokens, a case of a few GB)")
     ap.add_argument("--ep-tokens", type=int, default=0, help="tokens per rank of the split (0: the workload's)")
+    ap.add_argument("--ep-unit-rows", type=int, default=0,
+                    help="rows per transfer unit of the split (0: the emulated group's default)")
     return ap.parse_args()
 
 
@@ -676,7 +678,7 @@ def run_ours(a, w: wl.Workload):
         dist.destroy_process_group()
 
 
-def ep_split(dev, w, R, reps=20, n_b2b=20):
+def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
     """The expert-parallel split of the workload over R ranks emulated on this
     GPU (each rank its own seeded batch of w.T tokens, its own pool and a
     worst-case receive buffer): per step every rank plans and dispatches, the
@@ -690,7 +692,8 @@ def ep_split(dev, w, R, reps=20, n_b2b=20):
     the HBM copy peak, and the host scheduling time."""
     import torch
     from combine_moe_plan_gb300 import ep
-    g = ep.EmulatedGroup(R, w.T, w.H, w.E, w.P, w.k, device=dev)
+    kw = {"desc_kw": {"unit_rows": (unit_rows, unit_rows)}} if unit_rows else {}
+    g = ep.EmulatedGroup(R, w.T, w.H, w.E, w.P, w.k, device=dev, **kw)
     inps = [wl.make_inputs(w, seed=r, with_expert_out=False) for r in range(R)]
     logits = [torch.from_numpy(i["logits"]).to(dev) for i in inps]
     xs = [torch.from_numpy(i["x"].view(np.int16)).to(dev).view(torch.bfloat16) for i in inps]
@@ -825,7 +828,8 @@ def run_ep_only(a, w):
     torch.cuda.set_device(dev)
     if a.ep_tokens:
         w = wl.small_variant(w, a.ep_tokens)
-    print(json.dumps({"ep_split_emulated": ep_split(dev, w, a.ep_ranks, reps=a.steps)}), flush=True)
+    print(json.dumps({"ep_split_emulated": ep_split(dev, w, a.ep_ranks, reps=a.steps, unit_rows=a.ep_unit_rows)}),
+          flush=True)
 
 
 def main():

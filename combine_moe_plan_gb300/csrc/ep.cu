@@ -17,9 +17,14 @@
 // and 16-byte stores.  A unit is one contiguous run of rows in both buffers
 // (a piece of one peer's window of one expert), so a plane of a unit is a
 // plain memcpy; the schedule decides which core moves what, in which order.
+#include <unistd.h>
+
 #include <algorithm>
+#include <atomic>
+#include <condition_variable>
 #include <cstring>
 #include <functional>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -115,6 +120,86 @@ ep_pull_kernel(const moe_ep_unit* __restrict__ units, const int32_t* __restrict_
         }
     }
 }
+
+// ------------------------------------------------------------ workers ----
+
+// A few host threads kept for the scheduler's group calls, so that a call
+// does not pay for creating threads.  Created on first use and kept until the
+// process exits (detached: nothing is joined at exit).  One group call uses
+// them at a time; a call that finds them busy, or a process forked after they
+// were created (the child has none of them), runs its tasks on its own thread.
+class Workers {
+  public:
+    static Workers& get() {
+        static Workers* w = new Workers();  // never destroyed
+        return *w;
+    }
+
+    // task(i) for every i in [0, n), on the workers and the calling thread;
+    // returns once all have finished.  task must not throw.
+    void run(int n, const std::function<void(int)>& task) {
+        std::unique_lock<std::mutex> busy(run_mu_, std::try_to_lock);
+        if (!busy.owns_lock() || getpid() != owner_pid_ || threads_ == 0) {
+            for (int i = 0; i < n; ++i) task(i);
+            return;
+        }
+        {
+            std::lock_guard<std::mutex> lock(mu_);
+            task_ = &task;
+            n_ = n;
+            next_ = 0;
+            running_ = threads_;
+            ++generation_;
+        }
+        cv_work_.notify_all();
+        drain();
+        std::unique_lock<std::mutex> lock(mu_);
+        cv_done_.wait(lock, [&] { return running_ == 0; });
+        task_ = nullptr;
+    }
+
+  private:
+    Workers() : owner_pid_(getpid()) {
+        const unsigned hw = std::thread::hardware_concurrency();
+        const int want = (int)std::min<unsigned>(hw > 1 ? hw - 1 : 0, 15);
+        for (int i = 0; i < want; ++i) {
+            try {
+                std::thread(&Workers::loop, this).detach();
+                ++threads_;
+            } catch (...) {
+                break;  // fewer workers; the caller takes the rest
+            }
+        }
+    }
+
+    void drain() {
+        for (int i = next_++; i < n_; i = next_++) (*task_)(i);
+    }
+
+    void loop() {
+        uint64_t seen = 0;
+        for (;;) {
+            {
+                std::unique_lock<std::mutex> lock(mu_);
+                cv_work_.wait(lock, [&] { return generation_ != seen; });
+                seen = generation_;
+            }
+            drain();
+            std::lock_guard<std::mutex> lock(mu_);
+            if (--running_ == 0) cv_done_.notify_all();
+        }
+    }
+
+    std::mutex run_mu_, mu_;
+    std::condition_variable cv_work_, cv_done_;
+    const std::function<void(int)>* task_ = nullptr;
+    int n_ = 0;
+    std::atomic<int> next_{0};
+    int running_ = 0;
+    uint64_t generation_ = 0;
+    int threads_ = 0;
+    const pid_t owner_pid_;
+};
 
 // ------------------------------------------------------------ schedule ----
 
@@ -348,9 +433,13 @@ MOE_API int moe_ep_schedule(const moe_ep_desc* desc, int32_t direction, int32_t 
     if (rc != MOE_OK) return rc;
     if (puller < 0 || puller >= desc->R) return MOE_ERR_SIZE;
     Windows win;
-    if ((rc = win.build(desc->R, desc->P, counts)) != MOE_OK) return rc;
     Schedule out;
-    schedule_one(*desc, win, counts, direction, puller, row_bytes, &out);
+    try {  // no exception leaves the C ABI: an allocation failure is a size error
+        if ((rc = win.build(desc->R, desc->P, counts)) != MOE_OK) return rc;
+        schedule_one(*desc, win, counts, direction, puller, row_bytes, &out);
+    } catch (...) {
+        return MOE_ERR_SIZE;
+    }
     if ((int64_t)out.units.size() > max_units) return MOE_ERR_SIZE;
     std::copy(out.units.begin(), out.units.end(), units);
     std::copy(out.core_off.begin(), out.core_off.end(), core_off);
@@ -367,17 +456,25 @@ MOE_API int moe_ep_schedule_group(const moe_ep_desc* desc, int32_t direction, co
     if (rc != MOE_OK) return rc;
     const int32_t R = desc->R, C = desc->cores;
     Windows win;
-    if ((rc = win.build(R, desc->P, counts)) != MOE_OK) return rc;
-    std::vector<Schedule> out((size_t)R);
-    // One puller per worker thread; each writes only its own Schedule.
-    const int32_t n_thr = std::max(1, std::min<int32_t>(R, (int32_t)std::thread::hardware_concurrency()));
-    auto work = [&](int32_t first) {
-        for (int32_t r = first; r < R; r += n_thr) schedule_one(*desc, win, counts, direction, r, row_bytes, &out[r]);
-    };
-    std::vector<std::thread> pool;
-    for (int32_t t = 1; t < n_thr; ++t) pool.emplace_back(work, t);
-    work(0);
-    for (auto& t : pool) t.join();
+    std::vector<Schedule> out;
+    // One puller per task on the worker threads; each writes only its own
+    // Schedule.  No exception leaves the C ABI: a failure in any task is a
+    // size error.
+    std::atomic<bool> failed{false};
+    try {
+        if ((rc = win.build(R, desc->P, counts)) != MOE_OK) return rc;
+        out.resize((size_t)R);
+        Workers::get().run(R, [&](int r) {
+            try {
+                schedule_one(*desc, win, counts, direction, r, row_bytes, &out[r]);
+            } catch (...) {
+                failed = true;
+            }
+        });
+    } catch (...) {
+        return MOE_ERR_SIZE;
+    }
+    if (failed) return MOE_ERR_SIZE;
     int64_t total = 0;
     for (const Schedule& sc : out) total += (int64_t)sc.units.size();
     if (total > max_units) return MOE_ERR_SIZE;

@@ -233,7 +233,6 @@ class EmulatedGroup:
         kw = dict(self.LOCAL_TIERS, fanout_cap=(cores, cores))
         kw.update(desc_kw or {})
         self.desc = make_desc(R, P, cores, **kw)
-        self._workers = None
         self.pools = [moe.Pool(T_max, H, E, P, k, n_sets=1, device=device) for _ in range(R)]
         self.views = [p.view(0) for p in self.pools]
         self.Gs = self.views[0]["scales"].shape[1]
@@ -278,14 +277,11 @@ class EmulatedGroup:
         """Host schedules of both exchanges for all R pullers, packed:
         (dispatch units, core_off), (combine units, core_off), recv rows."""
         H, Gs = self.H, self.Gs
-        if self._workers is None:  # the two directions side by side (the C calls release the GIL)
-            import concurrent.futures as cf
-            self._workers = cf.ThreadPoolExecutor(max_workers=2)
-        fd = self._workers.submit(schedule_group, self.desc, 0, counts, H + 4 * Gs)
-        fc = self._workers.submit(schedule_group, self.desc, 1, counts, 2 * H)
+        disp = schedule_group(self.desc, 0, counts, H + 4 * Gs)[:2]  # each on libmoe's worker threads
+        comb = schedule_group(self.desc, 1, counts, 2 * H)[:2]
         owner = (np.arange(self.P, dtype=np.int64) * self.R) // self.P
         recv_rows = np.bincount(owner, weights=counts.sum(axis=0), minlength=self.R).astype(np.int64).tolist()
-        return fd.result()[:2], fc.result()[:2], [int(v) for v in recv_rows]
+        return disp, comb, [int(v) for v in recv_rows]
 
     def upload(self, packed, stream=None):
         """Host schedule arrays -> device tensors, copied on `stream`."""

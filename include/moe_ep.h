@@ -137,8 +137,10 @@ MOE_API int moe_ep_schedule(const moe_ep_desc* desc, int32_t direction, int32_t 
 
 /*
  * The schedules of all R pullers of a group in one call (the same schedule
- * moe_ep_schedule gives each puller), computed on up to R host threads and
- * packed: puller r's core c runs units[core_off[r, c] .. core_off[r, c+1])
+ * moe_ep_schedule gives each puller), computed on host worker threads the
+ * library starts on first use and keeps until the process exits (a call made
+ * while another one uses them, or in a process forked after they started,
+ * computes on the calling thread), and packed: puller r's core c runs units[core_off[r, c] .. core_off[r, c+1])
  * with absolute indices, ready for moe_ep_pull with first_puller 0 and
  * n_pullers R.
  *   units        host moe_ep_unit [max_units] (all pullers together)

@@ -199,3 +199,45 @@ def test_argument_checks():
     assert L.moe_dequant_rows(dev, dev, 4, 256, 2, dev, None) == -2
     assert L.moe_dequant_rows(None, dev, 4, 256, 4, dev, None) == -1
     assert L.moe_dequant_rows(None, None, 0, 256, 4, None, None) == 0
+
+
+@pytest.mark.filterwarnings("ignore:This process .* is multi-threaded:DeprecationWarning")
+def test_group_schedules_from_two_threads_at_once_and_after_fork():
+    """The group call's worker threads serve one call at a time; a call that
+    finds them busy computes on its own thread, and so does a process forked
+    after they started.  Every result equals the per-puller schedules."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    rng = np.random.default_rng(77)
+    R, P = 8, 288
+    counts = rng.integers(0, 400, size=(R, P)).astype(np.int32)
+    desc = ep.make_desc(R, P, 40)
+    want = {d: ep.pack_schedules([ep.schedule(desc, d, r, counts, 1000) for r in range(R)]) for d in (0, 1)}
+    ep.schedule_group(desc, 0, counts, 1000)  # the workers exist from here on
+
+    def one(d):
+        units, core_off, _ = ep.schedule_group(desc, d, counts, 1000)
+        return d, units, core_off
+
+    with cf.ThreadPoolExecutor(4) as ex:
+        for d, units, core_off in ex.map(one, [0, 1, 0, 1, 1, 0, 0, 1] * 3):
+            np.testing.assert_array_equal(units, want[d][0])
+            np.testing.assert_array_equal(core_off, want[d][1])
+    import torch
+    if torch.cuda.is_available() and torch.cuda.is_initialized():
+        return  # no fork once a CUDA context exists in this process
+    ctx = mp.get_context("fork")
+    q = ctx.Queue()
+    p = ctx.Process(target=_forked_group_call, args=(q, counts))
+    p.start()
+    units, core_off = q.get(timeout=120)
+    p.join(timeout=60)
+    assert p.exitcode == 0
+    np.testing.assert_array_equal(units, want[0][0])
+    np.testing.assert_array_equal(core_off, want[0][1])
+
+
+def _forked_group_call(q, counts):
+    desc = ep.make_desc(8, 288, 40)
+    units, core_off, _ = ep.schedule_group(desc, 0, counts, 1000)
+    q.put((units, core_off))
