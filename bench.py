@@ -705,37 +705,48 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
         t.copy_(torch.randn(t.shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16))
     s = torch.cuda.current_stream(dev)
     sched_s = []
+    ys = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
 
-    def one_step():
+    def one_step(fused):
         ev = g.plan_dispatch(logits, xs, ro, ri)
         counts = g.counts_host(ev)
         t0 = time.perf_counter()
         disp, comb, recv_rows = g.schedules(counts)
+        starts = g.recv_starts(counts) if fused else None
         sched_s.append(time.perf_counter() - t0)
         du, dc = g.upload(disp)
         cu, cc = g.upload(comb)
         g.pull_dispatch(du, dc)
-        g.pull_combine(cu, cc)
-        g.combine([w.T] * R)
-        return (du, dc, cu, cc), recv_rows, counts
+        if fused:
+            g.combine_fused([w.T] * R, recv_rows, starts, ys=ys)
+        else:
+            g.pull_combine(cu, cc)
+            g.combine([w.T] * R, ys=ys)
+        return (du, dc, cu, cc, starts), recv_rows, counts
 
-    for _ in range(3):
-        one_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    sched_s.clear()
-    e0.record(s)
-    for _ in range(reps):
-        packed, recv_rows, counts = one_step()
-    e1.record(s)
-    torch.cuda.synchronize()
-    step_ms = e0.elapsed_time(e1) / reps
+    def timed_steps(fused):
+        for _ in range(3):
+            one_step(fused)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        sched_s.clear()
+        e0.record(s)
+        for _ in range(reps):
+            out = one_step(fused)
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps, 1e3 * statistics.median(sched_s), out
 
-    du, dc, cu, cc = packed
+    fused_ms, _, (fused_packed, _, _) = timed_steps(True)
+    starts = fused_packed[4]
+    step_ms, sched_ms, (packed, recv_rows, counts) = timed_steps(False)
+
+    du, dc, cu, cc, _ = packed
     b2b = {}
     for name, fn in (("dispatch_pull", lambda: g.pull_dispatch(du, dc)),
-                     ("combine_pull", lambda: g.pull_combine(cu, cc))):
+                     ("combine_pull", lambda: g.pull_combine(cu, cc)),
+                     ("fused_combine_all_ranks", lambda: g.combine_fused([w.T] * R, recv_rows, starts, ys=ys))):
         for _ in range(3):
             fn()
         a0 = torch.cuda.Event(enable_timing=True)
@@ -749,13 +760,18 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
     if g.check() != 0:
         raise RuntimeError("device error word set in the split pass")
     rows = int(sum(recv_rows))
-    moved = {"dispatch_pull": 2 * rows * (w.H + 4 * g.Gs), "combine_pull": 2 * rows * 2 * w.H}
+    moved = {"dispatch_pull": 2 * rows * (w.H + 4 * g.Gs), "combine_pull": 2 * rows * 2 * w.H,
+             "fused_combine_all_ranks": R * w.algorithmic_bytes()["combine"]}
     peak, peak_src = _peaks()
     out = {"ranks": R, "workload_per_rank": w.name, "cores_per_puller": g.cores,
            "desc": {"fanout_cap": list(g.desc.fanout_cap), "unit_rows": list(g.desc.unit_rows),
                     "alpha_ns": list(g.desc.alpha_ns), "beta_gbs": list(g.desc.beta_gbs)},
            "value": R * w.T / (step_ms * 1e-3), "unit": "tokens/s (all ranks)", "ms_per_step": step_ms,
-           "host_schedule_ms_per_step": 1e3 * statistics.median(sched_s),
+           "fused_combine": {"value": R * w.T / (fused_ms * 1e-3), "ms_per_step": fused_ms,
+                             "what": "the combine reads each copy's row in its owner's receive buffer and "
+                                     "reduces locally (moe_ep_combine), instead of the combine pull and "
+                                     "moe_combine"},
+           "host_schedule_ms_per_step": sched_ms,
            "rows_exchanged": rows, "kernel_us_back_to_back": b2b,
            "pull_roofline": {k: {"bytes": moved[k], "achieved_gbs": moved[k] / (b2b[k] * 1e-6) / 1e9,
                                  "peak": peak, "frac": moved[k] / (b2b[k] * 1e-6) / 1e9 / peak}

@@ -374,6 +374,93 @@ void schedule_one(const moe_ep_desc& desc, const Windows& w, const int32_t* coun
     out->makespan = nu ? *std::max_element(load.begin(), load.end()) : 0;
 }
 
+// ------------------------------------------------------- fused combine ----
+
+constexpr int kCombineThreads = 256;  // 8 warps; one warp per (token, 256 elements)
+constexpr int kCombineSeg = 256;      // 32 lanes x 8 bf16 (16 bytes a lane)
+
+struct RecvTable {
+    const uint16_t* ex[MOE_EP_MAX_RANKS];  // each owner's bf16 receive rows
+    int64_t rows[MOE_EP_MAX_RANKS];
+};
+
+// Lane j < k of a warp holds copy j of token t: its owner's row address and
+// gate.  KB copies' 16-byte loads are in flight per lane before they are
+// accumulated in ascending j, as in the single-GPU combine.
+template <int KB>
+__global__ void __launch_bounds__(kCombineThreads)
+ep_combine_kernel(const int32_t* __restrict__ slot, const float* __restrict__ gates,
+                  const int32_t* __restrict__ phys, const int32_t* __restrict__ offsets,
+                  const int32_t* __restrict__ recv_start, int T, int H, int k, int R, int P, const RecvTable tab,
+                  uint16_t* __restrict__ y, int32_t* __restrict__ err) {
+    grid_dependency_sync();
+    const int lane = threadIdx.x & 31;
+    const int segs = (H + kCombineSeg - 1) / kCombineSeg;
+    const long long item = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5);
+    const int t = (int)(item / segs);
+    const int seg = (int)(item - (long long)t * segs);
+    if (t >= T) return;
+
+    unsigned long long src = 0;  // address of this lane's copy's row
+    float g = 0.0f;
+    bool bad = false;
+    if (lane < k) {
+        const int r = slot[(size_t)t * k + lane];
+        const int p = phys[(size_t)t * k + lane];
+        g = gates[(size_t)t * k + lane];
+        if (p < 0 || p >= P) {
+            bad = true;
+        } else {
+            const int d = (int)(((long long)p * R) / P);
+            const long long row = (long long)recv_start[p] + r - offsets[p];
+            if (row < 0 || row >= tab.rows[d] || tab.ex[d] == nullptr)
+                bad = true;
+            else
+                src = reinterpret_cast<unsigned long long>(tab.ex[d] + row * H);
+        }
+    }
+    if (__any_sync(kFull, bad)) {  // warp-uniform: skip the token's segment
+        if (lane == 0) set_error(err, MOE_DEVERR_UNIT);
+        return;
+    }
+    const int col = (seg * 32 + lane) * 8;
+    const bool act = col < H;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    for (int jb = 0; jb < k; jb += KB) {
+        uint4 d[KB];
+#pragma unroll
+        for (int jj = 0; jj < KB; ++jj) {
+            const int j = jb + jj;
+            const unsigned long long a = __shfl_sync(kFull, src, j & 31);
+            d[jj] = make_uint4(0, 0, 0, 0);
+            if (j < k && act) d[jj] = ld_stream16(reinterpret_cast<const uint16_t*>(a) + col);
+        }
+#pragma unroll
+        for (int jj = 0; jj < KB; ++jj) {
+            const int j = jb + jj;
+            const float gj = __shfl_sync(kFull, g, j & 31);
+            if (j < k) {
+                const uint32_t w[4] = {d[jj].x, d[jj].y, d[jj].z, d[jj].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = __fmaf_rn(gj, bf16_lo(w[i]), acc[2 * i]);
+                    acc[2 * i + 1] = __fmaf_rn(gj, bf16_hi(w[i]), acc[2 * i + 1]);
+                }
+            }
+        }
+    }
+    if (act) {
+        uint4 o;
+        o.x = pack_bf16x2_rn(acc[0], acc[1]);
+        o.y = pack_bf16x2_rn(acc[2], acc[3]);
+        o.z = pack_bf16x2_rn(acc[4], acc[5]);
+        o.w = pack_bf16x2_rn(acc[6], acc[7]);
+        st16(y + (size_t)t * H + col, o);
+    }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -519,6 +606,74 @@ MOE_API int moe_ep_pull(const moe_ep_unit* units, const int32_t* core_off, int32
                                static_cast<cudaStream_t>(stream), units, core_off, n_units, R, cores,
                                first_puller, pl, error_word);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+MOE_API int moe_ep_recv_start(int32_t R, int32_t P, const int32_t* counts, int32_t s, int32_t* recv_start) {
+    if (counts == nullptr || recv_start == nullptr) return MOE_ERR_NULL;
+    int rc = check_group(R, P);
+    if (rc != MOE_OK) return rc;
+    if (s < 0 || s >= R) return MOE_ERR_SIZE;
+    for (int32_t d = 0; d < R; ++d) {
+        int64_t row = 0;  // running row of d's receive buffer
+        for (int32_t p = rank_first_expert(d, R, P); p < rank_first_expert(d + 1, R, P); ++p)
+            for (int32_t q = 0; q < R; ++q) {
+                const int32_t n = counts[(size_t)q * P + p];
+                if (n < 0) return MOE_ERR_SIZE;
+                if (q == s) recv_start[p] = (int32_t)row;
+                row += n;
+                if (row > INT32_MAX) return MOE_ERR_SIZE;
+            }
+    }
+    return MOE_OK;
+}
+
+MOE_API int moe_ep_combine(moe_pool* pool, int32_t T, int buf, int32_t R, const uint16_t* const* recv_ex,
+                           const int64_t* recv_rows, const int32_t* recv_start, uint16_t* y, void* stream) {
+    if (pool == nullptr || recv_ex == nullptr || recv_rows == nullptr) return MOE_ERR_NULL;
+    const moe_desc& d = pool->geo.d;
+    if (buf < 0 || buf >= d.n_sets) return MOE_ERR_BUF;
+    if (T < 0 || T > d.T_max || R < 1 || R > MOE_EP_MAX_RANKS) return MOE_ERR_SIZE;
+    if (pool->planned_T[buf] != T) return MOE_ERR_STATE;
+    if (T == 0) return MOE_OK;
+    if (recv_start == nullptr || y == nullptr) return MOE_ERR_NULL;
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(recv_start) || misaligned(y)) return MOE_ERR_ALIGN;
+    RecvTable tab;
+    std::memset(&tab, 0, sizeof(tab));
+    for (int q = 0; q < R; ++q) {
+        if (recv_rows[q] < 0) return MOE_ERR_SIZE;
+        if (misaligned(recv_ex[q])) return MOE_ERR_ALIGN;
+        tab.ex[q] = recv_ex[q];
+        tab.rows[q] = recv_ex[q] == nullptr ? 0 : recv_rows[q];
+    }
+    const SetLayout& L = pool->geo.set[buf];
+    char* base = pool->base;
+    const int32_t* slot = reinterpret_cast<const int32_t*>(base + L.slot);
+    const float* gates = reinterpret_cast<const float*>(base + L.gates);
+    const int32_t* phys = reinterpret_cast<const int32_t*>(base + L.phys);
+    const int32_t* offsets = reinterpret_cast<const int32_t*>(base + L.offsets);
+    int32_t* err = reinterpret_cast<int32_t*>(base + pool->geo.error_word);
+    const long long items = (long long)T * ((d.H + kCombineSeg - 1) / kCombineSeg);
+    const dim3 grid((unsigned)((items + (kCombineThreads / 32) - 1) / (kCombineThreads / 32)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+#define MOE_EP_COMBINE_CASE(KB)                                                                              \
+    e = launch_pdl(ep_combine_kernel<KB>, grid, dim3(kCombineThreads), 0, s, slot, gates, phys, offsets,      \
+                   recv_start, T, d.H, d.k, R, d.P, tab, y, err)
+    switch (d.k < 8 ? d.k : 8) {
+        case 1: MOE_EP_COMBINE_CASE(1); break;
+        case 2: MOE_EP_COMBINE_CASE(2); break;
+        case 3: MOE_EP_COMBINE_CASE(3); break;
+        case 4: MOE_EP_COMBINE_CASE(4); break;
+        case 5: MOE_EP_COMBINE_CASE(5); break;
+        case 6: MOE_EP_COMBINE_CASE(6); break;
+        case 7: MOE_EP_COMBINE_CASE(7); break;
+        default: MOE_EP_COMBINE_CASE(8); break;
+    }
+#undef MOE_EP_COMBINE_CASE
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    pool->launches += 1;
+    return MOE_OK;
 }
 
 MOE_API int moe_dequant_rows(const int8_t* codes, const float* scales, int32_t rows, int32_t H,

@@ -58,6 +58,8 @@ def lib():
             "moe_ep_schedule_group": [pp(EpDesc), i32, vp, i64, vp, i32, pp(i32), vp, vp],
             "moe_ep_pull": [vp, vp, i32, i32, i32, i32, i32, pp(Plane), i32, vp, vp],
             "moe_dequant_rows": [vp, vp, i32, i32, i32, vp, vp],
+            "moe_ep_recv_start": [i32, i32, vp, i32, vp],
+            "moe_ep_combine": [vp, i32, ctypes.c_int, i32, pp(vp), pp(i64), vp, vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -166,6 +168,26 @@ def pull(units, core_off, R, cores, first_puller, n_pullers, planes, error_word,
     arr = (Plane * len(planes))(*planes)
     _call("moe_ep_pull", units.data_ptr() if units.numel() else None, core_off.data_ptr(), units.shape[0], R, cores,
           first_puller, n_pullers, arr, len(planes), error_word.data_ptr(), moe._stream(stream))
+
+
+def recv_start(counts, s):
+    """First row of rank s's window of every physical expert in its owner's
+    receive buffer (host int32 [P])."""
+    counts = np.ascontiguousarray(counts, np.int32)
+    R, P = counts.shape
+    out = np.zeros(P, np.int32)
+    _call("moe_ep_recv_start", R, P, _np_ptr(counts), s, _np_ptr(out))
+    return out
+
+
+def combine(pool, T, recv_ex, recv_rows, recv_start_dev, y, buf=0, stream=None):
+    """moe_ep_combine: rank's y [T, H] straight from the owners' receive buffers
+    (recv_ex: per-rank bf16 device tensors, recv_rows: rows each holds)."""
+    R = len(recv_ex)
+    ptrs = (vp * R)(*[None if t is None else t.data_ptr() for t in recv_ex])
+    rows = (i64 * R)(*[int(r) for r in recv_rows])
+    _call("moe_ep_combine", pool.handle, int(T), buf, R, ptrs, rows, recv_start_dev.data_ptr(), y.data_ptr(),
+          moe._stream(stream))
 
 
 def dequant_rows(codes, scales, rows, out, stream=None):
@@ -307,12 +329,31 @@ class EmulatedGroup:
         return [pool.combine(T, y=None if ys is None else ys[r], stream=stream)
                 for r, (pool, T) in enumerate(zip(self.pools, T_list))]
 
-    def step(self, logits, xs, rep_off=None, rep_ids=None, recv_ex_out=None, stream=None):
+    def recv_starts(self, counts, stream=None):
+        """Every rank's recv_start table [R, P] on the device (copied on `stream`)."""
+        tab = np.stack([recv_start(counts, s) for s in range(self.R)])
+        s = stream or torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(s):
+            return torch.from_numpy(tab).pin_memory().to(self.device, non_blocking=True)
+
+    def combine_fused(self, T_list, recv_rows, starts, ys=None, stream=None):
+        """Every rank's y straight from the owners' receive buffers (no
+        combine pull): moe_ep_combine per rank."""
+        out = []
+        for r, (pool, T) in enumerate(zip(self.pools, T_list)):
+            y = ys[r] if ys is not None else torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device)
+            combine(pool, T, self.recv_ex, recv_rows, starts[r], y, stream=stream)
+            out.append(y)
+        return out
+
+    def step(self, logits, xs, rep_off=None, rep_ids=None, recv_ex_out=None, stream=None, fused_combine=False):
         """The whole split path: plan + dispatch on every rank, counts to the
         host, schedules, the dispatch pull, the experts (identity experts on
         the receive buffers unless recv_ex_out[d] gives each receiver's bf16
-        rows), the combine pull, and every rank's combine.  Returns the
-        per-rank y and the counts."""
+        rows), the combine pull, and every rank's combine -- or, with
+        fused_combine, every rank's moe_ep_combine straight from the owners'
+        receive buffers instead of the combine pull and moe_combine.  Returns
+        the per-rank y, the counts and the rows each rank received."""
         ev = self.plan_dispatch(logits, xs, rep_off, rep_ids, stream)
         counts = self.counts_host(ev)
         disp, comb, recv_rows = self.schedules(counts)
@@ -324,8 +365,12 @@ class EmulatedGroup:
         else:
             for d in range(self.R):
                 self.recv_ex[d][:recv_rows[d]].copy_(recv_ex_out[d])
-        self.pull_combine(cu, cc, stream)
-        ys = self.combine([lg.shape[0] for lg in logits], stream=stream)
+        T_list = [lg.shape[0] for lg in logits]
+        if fused_combine:
+            ys = self.combine_fused(T_list, recv_rows, self.recv_starts(counts, stream), stream=stream)
+        else:
+            self.pull_combine(cu, cc, stream)
+            ys = self.combine(T_list, stream=stream)
         return ys, counts, recv_rows
 
     def check(self) -> int:

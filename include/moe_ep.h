@@ -197,6 +197,38 @@ MOE_API int moe_ep_pull(const moe_ep_unit* units, const int32_t* core_off, int32
                         int32_t n_planes, int32_t* error_word, void* stream);
 
 /*
+ * Where rank s's copies of each expert sit in the expert's owner's receive
+ * buffer (StrataCL section 3.5 layout, as moe_ep_layout):
+ *   recv_start  host int32 [P]: for physical expert p owned by rank d, the
+ *               first row of source s's window of p in d's receive buffer
+ * (0 where s routed nothing to p).  Host only.
+ */
+MOE_API int moe_ep_recv_start(int32_t R, int32_t P, const int32_t* counts, int32_t s, int32_t* recv_start);
+
+/*
+ * Fused combine of rank s (a pull-mode reduction, StrataCL section 3.4:
+ * remote operands loaded on chip and accumulated into the local output;
+ * CloudMatrix384 write-up, "FusedDispatch and FusedCombine": expert output
+ * return and weighted reduce in one operator).  For every token t of the
+ * pool's set `buf` (planned with T tokens on rank s), and j = 0..k-1 in
+ * ascending order, the copy's expert output row is read straight from its
+ * owner's receive buffer -- row recv_start[p] + slot[t, j] - offsets[p] of
+ * rank floor(p * R / P)'s buffer, p = phys[t, j] -- and accumulated with
+ * fmaf(gate, row, acc) in fp32; y[t] = bf16(acc).  The result equals a
+ * combine pull (moe_ep_pull, direction 1) followed by moe_combine, bit for
+ * bit, without writing the rows back.
+ *   recv_ex    host array [R] of device addresses: each owner's bf16 [rows, H]
+ *              expert outputs (NULL with 0 rows for a rank that owns none)
+ *   recv_rows  host int64 [R]: rows of each owner's buffer (bounds)
+ *   recv_start device int32 [P] (moe_ep_recv_start of rank s)
+ *   y          device bf16 [T, H]
+ * A row outside its owner's buffer is skipped and sets MOE_DEVERR_UNIT in the
+ * pool's error word.  Requires a prior moe_plan on this set with the same T.
+ */
+MOE_API int moe_ep_combine(moe_pool* pool, int32_t T, int buf, int32_t R, const uint16_t* const* recv_ex,
+                           const int64_t* recv_rows, const int32_t* recv_start, uint16_t* y, void* stream);
+
+/*
  * Dequantize rows (the identity-expert stand-in on any buffer, e.g. a
  * receive buffer): out[r, i] = bf16(codes[r, i] * scales[r, i / 128]) for
  * r < rows (CloudMatrix384 write-up, "FusedDispatch and FusedCombine": INT8

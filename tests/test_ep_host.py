@@ -241,3 +241,41 @@ def _forked_group_call(q, counts):
     desc = ep.make_desc(8, 288, 40)
     units, core_off, _ = ep.schedule_group(desc, 0, counts, 1000)
     q.put((units, core_off))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_recv_start_follows_the_oracle_layout(seed):
+    rng = np.random.default_rng(300 + seed)
+    R = int(rng.integers(1, 9))
+    P = int(rng.integers(1, 40))
+    counts = rng.integers(0, 50, size=(R, P)).astype(np.int32)
+    counts[rng.random((R, P)) < 0.2] = 0
+    for s in range(R):
+        st = ep.recv_start(counts, s)
+        for d in range(R):
+            _, chunk = oracle.ep_layout(counts, d)
+            mine = [p for p in range(P) if oracle.ep_owner(p, R, P) == d]
+            for i, p in enumerate(mine):
+                assert st[p] == chunk[s, i]
+
+
+def test_fused_combine_checks_before_launch():
+    """moe_ep_combine rejects bad arguments on the host (no GPU here: a call
+    that got past the checks could only fail with MOE_ERR_CUDA, -6)."""
+    import ctypes
+    from combine_moe_plan_gb300 import moe
+    L = ep.lib()
+    d = moe.Desc(64, 256, 8, 8, 2, 128, 1)
+    n = ctypes.c_size_t()
+    assert L.moe_pool_bytes(ctypes.byref(d), ctypes.byref(n)) == 0
+    h = ctypes.c_void_p()
+    assert L.moe_pool_init(ctypes.byref(d), ctypes.c_void_p(1 << 40), n.value, ctypes.byref(h)) == 0
+    ptrs = (ctypes.c_void_p * 2)(1 << 41, 1 << 41)
+    rows = (ctypes.c_int64 * 2)(10, 10)
+    good = ctypes.c_void_p(1 << 41)
+    assert L.moe_ep_combine(None, 8, 0, 2, ptrs, rows, good, good, None) == -1
+    assert L.moe_ep_combine(h, 8, 1, 2, ptrs, rows, good, good, None) == -4     # no set 1
+    assert L.moe_ep_combine(h, 65, 0, 2, ptrs, rows, good, good, None) == -2    # T > T_max
+    assert L.moe_ep_combine(h, 8, 0, 65, ptrs, rows, good, good, None) == -2    # R too large
+    assert L.moe_ep_combine(h, 8, 0, 2, ptrs, rows, good, good, None) == -9     # no plan on this set
+    L.moe_pool_destroy(h)

@@ -33,7 +33,7 @@ def _inputs(w, R, Ts=None, seed0=0):
     return out
 
 
-def _check(g, inps, w, recv_rows, ys, counts, ref=None, recv_ex_out=None):
+def _check(g, inps, w, recv_rows, ys, counts, ref=None, recv_ex_out=None, fused=False):
     R = g.R
     rep_off, rep_ids = inps[0]["rep_off"], inps[0]["rep_ids"]
     if ref is None:
@@ -48,7 +48,9 @@ def _check(g, inps, w, recv_rows, ys, counts, ref=None, recv_ex_out=None):
                                       f32_bits(ref["recv_scales"][d]), err_msg=f"scales {d}")
     for s in range(R):
         rows = int(counts[s].sum())
-        np.testing.assert_array_equal(host_u16(g.views[s]["ex_out"][:rows]), ref["ex_out"][s], err_msg=f"ex_out {s}")
+        if not fused:  # the fused combine reads the owners' rows in place: nothing comes back to the pool
+            np.testing.assert_array_equal(host_u16(g.views[s]["ex_out"][:rows]), ref["ex_out"][s],
+                                          err_msg=f"ex_out {s}")
         assert_y_close(host_u16(ys[s]), ref["y"][s], f"y of rank {s}")
     assert g.check() == 0
 
@@ -57,27 +59,29 @@ def _group(w, R, **kw):
     return ep.EmulatedGroup(R, max(w.T, 1), w.H, w.E, w.P, w.k, **kw)
 
 
-def _run(g, inps, recv_ex_out=None):
+def _run(g, inps, recv_ex_out=None, fused=False):
     logits = [dev(i["logits"]) for i in inps]
     xs = [dev_bf16(i["x"]) for i in inps]
     ro = None if inps[0]["rep_off"] is None else dev(inps[0]["rep_off"])
     ri = None if inps[0]["rep_ids"] is None else dev(inps[0]["rep_ids"])
     rex = None if recv_ex_out is None else [dev_bf16(a) for a in recv_ex_out]
-    ys, counts, recv_rows = g.step(logits, xs, ro, ri, recv_ex_out=rex)
+    ys, counts, recv_rows = g.step(logits, xs, ro, ri, recv_ex_out=rex, fused_combine=fused)
     torch.cuda.synchronize()
     return ys, counts, recv_rows
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("R,T,cores,cap,S", [(1, 96, 4, (8, 8), (64, 64)), (2, 150, 3, (1, 1), (5, 7)),
                                              (3, 77, 8, (2, 1), (16, 3)), (4, 64, 16, (8, 8), (1, 1))])
-def test_split_small_identity_experts(R, T, cores, cap, S):
+def test_split_small_identity_experts(R, T, cores, cap, S, fused):
     """The bench workload's experts (288 physical, 32 replicas) at small
-    batches: many small units, caps that bind, single-row units."""
+    batches: many small units, caps that bind, single-row units; the combine
+    either pulled back then reduced, or fused (rows read in place)."""
     w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T), H=1024)
     inps = _inputs(w, R)
     g = _group(w, R, cores=cores, desc_kw=dict(fanout_cap=cap, unit_rows=S))
-    ys, counts, recv_rows = _run(g, inps)
-    _check(g, inps, w, recv_rows, ys, counts)
+    ys, counts, recv_rows = _run(g, inps, fused=fused)
+    _check(g, inps, w, recv_rows, ys, counts, fused=fused)
 
 
 def test_split_generated_expert_rows_and_ragged_batches():
@@ -94,6 +98,8 @@ def test_split_generated_expert_rows_and_ragged_batches():
     g = ep.EmulatedGroup(R, 300, w.H, w.E, w.P, w.k, cores=6)
     ys, counts, recv_rows = _run(g, inps, rex)
     _check(g, inps, w, recv_rows, ys, counts, recv_ex_out=rex)
+    ys, counts, recv_rows = _run(g, inps, rex, fused=True)
+    _check(g, inps, w, recv_rows, ys, counts, recv_ex_out=rex, fused=True)
 
 
 def test_split_more_ranks_than_experts_and_one_hot_expert():
@@ -107,21 +113,30 @@ def test_split_more_ranks_than_experts_and_one_hot_expert():
         i["logits"][:, 1] = 4.0
         i["logits"][:, 2] = 3.0
     g = _group(w, R, cores=3)
-    ys, counts, recv_rows = _run(g, inps)
-    assert sorted(recv_rows) == [0, 0, 0, 0, R * w.T, R * w.T]
-    _check(g, inps, w, recv_rows, ys, counts)
+    for fused in (False, True):
+        ys, counts, recv_rows = _run(g, inps, fused=fused)
+        assert sorted(recv_rows) == [0, 0, 0, 0, R * w.T, R * w.T]
+        _check(g, inps, w, recv_rows, ys, counts, fused=fused)
 
 
 def test_split_full_bench_shape_eight_ranks():
     """Eight ranks of the bench workload (4096 tokens x 7168, 256 experts + 32
     replicas, top-8) with the default group cost model: every receive buffer,
-    every returned row and every y compared in full."""
+    every returned row and every y compared in full; then the fused combine,
+    whose y must equal the pulled-back one bit for bit."""
     w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
     R = 8
     inps = _inputs(w, R)
     g = _group(w, R)
     ys, counts, recv_rows = _run(g, inps)
-    _check(g, inps, w, recv_rows, ys, counts)
+    ref = oracle.ep_forward([i["logits"] for i in inps], [i["x"] for i in inps], w.k, w.P, inps[0]["rep_off"],
+                            inps[0]["rep_ids"])
+    _check(g, inps, w, recv_rows, ys, counts, ref=ref)
+    ys_pulled = [y.clone() for y in ys]
+    ys, counts, recv_rows = _run(g, inps, fused=True)
+    _check(g, inps, w, recv_rows, ys, counts, ref=ref, fused=True)
+    for a, b in zip(ys, ys_pulled):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 def test_one_puller_per_launch_equals_all_pullers():
@@ -164,3 +179,20 @@ def test_bad_units_are_skipped_and_reported():
     assert int(err.item()) == ep.DEVERR_UNIT
     assert torch.equal(dst[0][:8], src[1][:8])
     assert int(dst[0][8:].abs().sum().item()) == 0 and int(dst[1].abs().sum().item()) == 0
+
+
+def test_fused_combine_rejects_rows_outside_the_owners_buffers():
+    """recv_start tables that point past an owner's rows: the fused combine
+    skips those tokens and reports MOE_DEVERR_UNIT; no access outside."""
+    w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 64), H=256)
+    R = 2
+    inps = _inputs(w, R)
+    g = _group(w, R, cores=2)
+    _, counts, recv_rows = _run(g, inps)
+    starts = g.recv_starts(counts)
+    starts[0].fill_(1 << 30)  # every expert window of rank 0 far past the end
+    y = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    ep.combine(g.pools[0], w.T, g.recv_ex, recv_rows, starts[0], y)
+    err = g.pools[0].check()
+    assert err & ep.DEVERR_UNIT
+    assert int((y.view(torch.int16) != 0).sum().item()) == 0
