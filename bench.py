@@ -707,7 +707,15 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
     sched_s = []
     ys = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
 
+    cap = [t.shape[0] for t in g.recv_ex]
+
     def one_step(fused):
+        if fused == "all":  # fused dispatch and combine: no schedule, no pull, no host round trip
+            g.plan_all(logits, ro, ri)
+            starts_dev, _ = g.starts_device()
+            g.dispatch_fused(xs, starts_dev)
+            g.combine_fused([w.T] * R, cap, starts_dev, ys=ys)
+            return None
         ev = g.plan_dispatch(logits, xs, ro, ri)
         counts = g.counts_host(ev)
         t0 = time.perf_counter()
@@ -736,17 +744,20 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
             out = one_step(fused)
         e1.record(s)
         torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps, 1e3 * statistics.median(sched_s), out
+        return e0.elapsed_time(e1) / reps, 1e3 * statistics.median(sched_s) if sched_s else 0.0, out
 
+    all_fused_ms, _, _ = timed_steps("all")
     fused_ms, _, (fused_packed, _, _) = timed_steps(True)
     starts = fused_packed[4]
     step_ms, sched_ms, (packed, recv_rows, counts) = timed_steps(False)
+    starts_dev, _ = g.starts_device()
 
     du, dc, cu, cc, _ = packed
     b2b = {}
     for name, fn in (("dispatch_pull", lambda: g.pull_dispatch(du, dc)),
                      ("combine_pull", lambda: g.pull_combine(cu, cc)),
-                     ("fused_combine_all_ranks", lambda: g.combine_fused([w.T] * R, recv_rows, starts, ys=ys))):
+                     ("fused_combine_all_ranks", lambda: g.combine_fused([w.T] * R, recv_rows, starts, ys=ys)),
+                     ("fused_dispatch_all_ranks", lambda: g.dispatch_fused(xs, starts_dev))):
         for _ in range(3):
             fn()
         a0 = torch.cuda.Event(enable_timing=True)
@@ -761,7 +772,8 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
         raise RuntimeError("device error word set in the split pass")
     rows = int(sum(recv_rows))
     moved = {"dispatch_pull": 2 * rows * (w.H + 4 * g.Gs), "combine_pull": 2 * rows * 2 * w.H,
-             "fused_combine_all_ranks": R * w.algorithmic_bytes()["combine"]}
+             "fused_combine_all_ranks": R * w.algorithmic_bytes()["combine"],
+             "fused_dispatch_all_ranks": R * w.algorithmic_bytes()["dispatch"]}
     peak, peak_src = _peaks()
     out = {"ranks": R, "workload_per_rank": w.name, "cores_per_puller": g.cores,
            "desc": {"fanout_cap": list(g.desc.fanout_cap), "unit_rows": list(g.desc.unit_rows),
@@ -771,6 +783,11 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
                              "what": "the combine reads each copy's row in its owner's receive buffer and "
                                      "reduces locally (moe_ep_combine), instead of the combine pull and "
                                      "moe_combine"},
+           "fused": {"value": R * w.T / (all_fused_ms * 1e-3), "ms_per_step": all_fused_ms,
+                     "what": "window starts on the device (moe_ep_recv_start_device), every rank's tokens "
+                             "quantized and written straight into the owners' receive buffers "
+                             "(moe_ep_dispatch), and the fused combine: no schedule, no pull, no host round "
+                             "trip"},
            "host_schedule_ms_per_step": sched_ms,
            "rows_exchanged": rows, "kernel_us_back_to_back": b2b,
            "pull_roofline": {k: {"bytes": moved[k], "achieved_gbs": moved[k] / (b2b[k] * 1e-6) / 1e9,

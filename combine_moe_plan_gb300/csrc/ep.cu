@@ -31,6 +31,7 @@
 #include "moe_ep.h"
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace moe {
 namespace {
@@ -461,6 +462,132 @@ ep_combine_kernel(const int32_t* __restrict__ slot, const float* __restrict__ ga
     }
 }
 
+// ------------------------------------------------ window starts, device ----
+
+constexpr int kStartThreads = 1024;
+
+struct CountsTable {
+    const int32_t* c[MOE_EP_MAX_RANKS];  // rank q's counts [P]
+};
+
+// One CTA: per expert the rows of all ranks (tot), their exclusive scan over
+// the experts, each expert's window start inside its owner's buffer (the scan
+// minus the scan at the owner's first expert), then each source's start
+// inside the window (the counts of the ranks before it added up).
+__global__ void __launch_bounds__(kStartThreads)
+ep_recv_start_kernel(const CountsTable tab, int R, int P, int32_t* __restrict__ recv_start,
+                     int32_t* __restrict__ recv_rows) {
+    extern __shared__ long long excl[];  // [P + 1]
+    __shared__ long long warp_tot[kStartThreads / 32];
+    grid_dependency_sync();
+    allow_dependents();
+    const int per = (P + kStartThreads - 1) / kStartThreads;
+    const int lo = threadIdx.x * per;
+    long long chunk = 0;
+    for (int p = lo; p < lo + per && p < P; ++p) {
+        long long tot = 0;
+        for (int q = 0; q < R; ++q) tot += tab.c[q][p];
+        excl[p] = tot;
+        chunk += tot;
+    }
+    // exclusive scan of the chunk totals over the CTA
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long incl = chunk;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    long long wsum = lane < kStartThreads / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_up_sync(kFull, wsum, off);
+        if (lane >= off) wsum += o;
+    }
+    long long run = __shfl_sync(kFull, wsum, warp) - warp_tot[warp] + incl - chunk;
+    __syncthreads();
+    for (int p = lo; p < lo + per && p < P; ++p) {
+        const long long v = excl[p];
+        excl[p] = run;
+        run += v;
+    }
+    if (threadIdx.x == kStartThreads - 1) excl[P] = run;
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += kStartThreads) {
+        const int d = (int)(((long long)p * R) / P);
+        const int first = (int)(((long long)d * P + R - 1) / R);
+        long long row = excl[p] - excl[first];
+        for (int s = 0; s < R; ++s) {
+            recv_start[(size_t)s * P + p] = (int32_t)row;
+            row += tab.c[s][p];
+        }
+    }
+    if (recv_rows != nullptr)
+        for (int d = threadIdx.x; d < R; d += kStartThreads) {
+            const int first = (int)(((long long)d * P + R - 1) / R);
+            const int last = (int)(((long long)(d + 1) * P + R - 1) / R);
+            recv_rows[d] = (int32_t)(excl[last] - excl[first]);
+        }
+}
+
+// ---------------------------------------------------------- fused dispatch ----
+
+constexpr int kDispatchThreads = 256;  // 8 warps, one per (token, 512-element segment)
+
+struct SendTable {
+    int8_t* codes[MOE_EP_MAX_RANKS];  // each owner's receive rows
+    float* scales[MOE_EP_MAX_RANKS];
+    int64_t rows[MOE_EP_MAX_RANKS];
+};
+
+// The dispatch of one rank written straight into the owners' receive
+// buffers: per warp, one segment of one token is loaded and quantized once
+// (quant.cuh), and lane j < k addresses copy j in its owner's buffer; the
+// codes leave as one 16-byte store per lane and copy, the segment's four
+// scales as one 16-byte store per copy.
+__global__ void __launch_bounds__(kDispatchThreads)
+ep_dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, int R, int P, int Gs,
+                   const int32_t* __restrict__ slot, const int32_t* __restrict__ phys,
+                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ recv_start, const SendTable tab,
+                   int32_t* __restrict__ err) {
+    grid_dependency_sync();
+    allow_dependents();
+    const int lane = threadIdx.x & 31;
+    const int segs = (H + kSegElems - 1) / kSegElems;
+    const long long item = (long long)blockIdx.x * (kDispatchThreads / 32) + (threadIdx.x >> 5);
+    const int t = (int)(item / segs);
+    const int seg = (int)(item - (long long)t * segs);
+    if (t >= T) return;
+    const SegLoad ld = load_segment(x, t, H, seg, lane);
+    unsigned long long cdst = 0;  // copy `lane`'s code row in its owner's buffer (0: skipped)
+    float* sdst = nullptr;
+    if (lane < k) {
+        const int r = slot[(size_t)t * k + lane];
+        const int p = phys[(size_t)t * k + lane];
+        long long row = -1;
+        int d = 0;
+        if (p >= 0 && p < P) {
+            d = (int)(((long long)p * R) / P);
+            row = (long long)recv_start[p] + r - offsets[p];
+        }
+        if (row < 0 || row >= tab.rows[d] || tab.codes[d] == nullptr || tab.scales[d] == nullptr) {
+            set_error(err, MOE_DEVERR_UNIT);
+        } else {
+            cdst = reinterpret_cast<unsigned long long>(tab.codes[d] + row * H);
+            sdst = tab.scales[d] + row * Gs;
+        }
+    }
+    const SegQuant qz = quantize_segment(ld);
+    for (int j = 0; j < k; ++j) {
+        const unsigned long long a = __shfl_sync(kFull, cdst, j);
+        if (a == 0) continue;  // warp-uniform
+        if (ld.active) st16(reinterpret_cast<int8_t*>(a) + (size_t)ld.chunk * 16, qz.q);
+    }
+    if (sdst != nullptr && seg * 4 < Gs) *reinterpret_cast<float4*>(sdst + seg * 4) = qz.sc;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -627,6 +754,65 @@ MOE_API int moe_ep_recv_start(int32_t R, int32_t P, const int32_t* counts, int32
     return MOE_OK;
 }
 
+MOE_API int moe_ep_recv_start_device(int32_t R, int32_t P, const int32_t* const* counts, int32_t* recv_start,
+                                     int32_t* recv_rows, void* stream) {
+    if (counts == nullptr || recv_start == nullptr) return MOE_ERR_NULL;
+    int rc = check_group(R, P);
+    if (rc != MOE_OK) return rc;
+    if ((reinterpret_cast<uintptr_t>(recv_start) & 3u) != 0 || (reinterpret_cast<uintptr_t>(recv_rows) & 3u) != 0)
+        return MOE_ERR_ALIGN;
+    CountsTable tab;
+    std::memset(&tab, 0, sizeof(tab));
+    for (int q = 0; q < R; ++q) {
+        if (counts[q] == nullptr) return MOE_ERR_NULL;
+        tab.c[q] = counts[q];
+    }
+    const size_t smem = (size_t)(P + 1) * sizeof(long long);
+    cudaError_t e = cudaSuccess;
+    if (smem > 48 * 1024)
+        e = cudaFuncSetAttribute(ep_recv_start_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = launch_pdl(ep_recv_start_kernel, dim3(1), dim3(kStartThreads), smem, static_cast<cudaStream_t>(stream),
+                       tab, R, P, recv_start, recv_rows);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, int32_t R,
+                            int8_t* const* recv_codes, float* const* recv_scales, const int64_t* recv_rows,
+                            const int32_t* recv_start, void* stream) {
+    if (pool == nullptr || recv_codes == nullptr || recv_scales == nullptr || recv_rows == nullptr)
+        return MOE_ERR_NULL;
+    const moe_desc& d = pool->geo.d;
+    if (buf < 0 || buf >= d.n_sets) return MOE_ERR_BUF;
+    if (T < 0 || T > d.T_max || R < 1 || R > MOE_EP_MAX_RANKS) return MOE_ERR_SIZE;
+    if (pool->planned_T[buf] != T) return MOE_ERR_STATE;
+    if (T == 0) return MOE_OK;
+    if (x == nullptr || recv_start == nullptr) return MOE_ERR_NULL;
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(x) || (reinterpret_cast<uintptr_t>(recv_start) & 3u) != 0) return MOE_ERR_ALIGN;
+    SendTable tab;
+    std::memset(&tab, 0, sizeof(tab));
+    for (int q = 0; q < R; ++q) {
+        if (recv_rows[q] < 0) return MOE_ERR_SIZE;
+        if (misaligned(recv_codes[q]) || misaligned(recv_scales[q])) return MOE_ERR_ALIGN;
+        tab.codes[q] = recv_codes[q];
+        tab.scales[q] = recv_scales[q];
+        tab.rows[q] = (recv_codes[q] == nullptr || recv_scales[q] == nullptr) ? 0 : recv_rows[q];
+    }
+    const SetLayout& L = pool->geo.set[buf];
+    char* base = pool->base;
+    const long long items = (long long)T * ((d.H + kSegElems - 1) / kSegElems);
+    const dim3 grid((unsigned)((items + (kDispatchThreads / 32) - 1) / (kDispatchThreads / 32)));
+    cudaError_t e = launch_pdl(ep_dispatch_kernel, grid, dim3(kDispatchThreads), 0, static_cast<cudaStream_t>(stream),
+                               x, T, d.H, d.k, R, d.P, pool->geo.Gs, reinterpret_cast<const int32_t*>(base + L.slot),
+                               reinterpret_cast<const int32_t*>(base + L.phys),
+                               reinterpret_cast<const int32_t*>(base + L.offsets), recv_start, tab,
+                               reinterpret_cast<int32_t*>(base + pool->geo.error_word));
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    pool->launches += 1;
+    return MOE_OK;
+}
+
 MOE_API int moe_ep_combine(moe_pool* pool, int32_t T, int buf, int32_t R, const uint16_t* const* recv_ex,
                            const int64_t* recv_rows, const int32_t* recv_start, uint16_t* y, void* stream) {
     if (pool == nullptr || recv_ex == nullptr || recv_rows == nullptr) return MOE_ERR_NULL;
@@ -637,7 +823,7 @@ MOE_API int moe_ep_combine(moe_pool* pool, int32_t T, int buf, int32_t R, const 
     if (T == 0) return MOE_OK;
     if (recv_start == nullptr || y == nullptr) return MOE_ERR_NULL;
     auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
-    if (misaligned(recv_start) || misaligned(y)) return MOE_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(recv_start) & 3u) != 0 || misaligned(y)) return MOE_ERR_ALIGN;
     RecvTable tab;
     std::memset(&tab, 0, sizeof(tab));
     for (int q = 0; q < R; ++q) {

@@ -59,6 +59,8 @@ def lib():
             "moe_ep_pull": [vp, vp, i32, i32, i32, i32, i32, pp(Plane), i32, vp, vp],
             "moe_dequant_rows": [vp, vp, i32, i32, i32, vp, vp],
             "moe_ep_recv_start": [i32, i32, vp, i32, vp],
+            "moe_ep_recv_start_device": [i32, i32, pp(vp), vp, vp, vp],
+            "moe_ep_dispatch": [vp, vp, i32, ctypes.c_int, i32, pp(vp), pp(vp), pp(i64), vp, vp],
             "moe_ep_combine": [vp, i32, ctypes.c_int, i32, pp(vp), pp(i64), vp, vp, vp],
         }
         for name, args in sig.items():
@@ -178,6 +180,27 @@ def recv_start(counts, s):
     out = np.zeros(P, np.int32)
     _call("moe_ep_recv_start", R, P, _np_ptr(counts), s, _np_ptr(out))
     return out
+
+
+def recv_start_device(counts_dev, recv_start_dev, recv_rows_dev=None, stream=None):
+    """moe_ep_recv_start_device: every rank's window starts [R, P] (and rows
+    received [R]) from the ranks' device counts, computed on the device."""
+    R = len(counts_dev)
+    P = counts_dev[0].shape[0]
+    ptrs = (vp * R)(*[t.data_ptr() for t in counts_dev])
+    _call("moe_ep_recv_start_device", R, P, ptrs, recv_start_dev.data_ptr(),
+          None if recv_rows_dev is None else recv_rows_dev.data_ptr(), moe._stream(stream))
+
+
+def dispatch(pool, x, recv_codes, recv_scales, recv_rows, recv_start_dev, buf=0, stream=None):
+    """moe_ep_dispatch: the rank's tokens quantized and written straight into
+    the owners' receive buffers."""
+    R = len(recv_codes)
+    cp = (vp * R)(*[None if t is None else t.data_ptr() for t in recv_codes])
+    sp = (vp * R)(*[None if t is None else t.data_ptr() for t in recv_scales])
+    rows = (i64 * R)(*[int(r) for r in recv_rows])
+    _call("moe_ep_dispatch", pool.handle, x.data_ptr() if x.numel() else None, x.shape[0], buf, R, cp, sp, rows,
+          recv_start_dev.data_ptr(), moe._stream(stream))
 
 
 def combine(pool, T, recv_ex, recv_rows, recv_start_dev, y, buf=0, stream=None):
@@ -346,14 +369,40 @@ class EmulatedGroup:
             out.append(y)
         return out
 
-    def step(self, logits, xs, rep_off=None, rep_ids=None, recv_ex_out=None, stream=None, fused_combine=False):
+    def plan_all(self, logits, rep_off=None, rep_ids=None, stream=None):
+        for pool, lg in zip(self.pools, logits):
+            pool.plan(lg, rep_off, rep_ids, stream=stream)
+
+    def starts_device(self, stream=None):
+        """Every rank's window starts [R, P] and rows received [R], computed on
+        the device from the plans' counts (moe_ep_recv_start_device)."""
+        if not hasattr(self, "_starts"):
+            self._starts = torch.empty((self.R, self.P), dtype=torch.int32, device=self.device)
+            self._rows = torch.empty(self.R, dtype=torch.int32, device=self.device)
+        recv_start_device([v["counts"] for v in self.views], self._starts, self._rows, stream)
+        return self._starts, self._rows
+
+    def dispatch_fused(self, xs, starts, stream=None):
+        """Every rank's fused dispatch into the owners' receive buffers."""
+        cap = [t.shape[0] for t in self.recv_codes]
+        for r, (pool, x) in enumerate(zip(self.pools, xs)):
+            dispatch(pool, x, self.recv_codes, self.recv_scales, cap, starts[r], stream=stream)
+
+    def step(self, logits, xs, rep_off=None, rep_ids=None, recv_ex_out=None, stream=None, fused_combine=False,
+             fused_dispatch=False):
         """The whole split path: plan + dispatch on every rank, counts to the
         host, schedules, the dispatch pull, the experts (identity experts on
         the receive buffers unless recv_ex_out[d] gives each receiver's bf16
         rows), the combine pull, and every rank's combine -- or, with
         fused_combine, every rank's moe_ep_combine straight from the owners'
-        receive buffers instead of the combine pull and moe_combine.  Returns
-        the per-rank y, the counts and the rows each rank received."""
+        receive buffers instead of the combine pull and moe_combine.  With
+        fused_dispatch (which implies fused_combine) the window starts are
+        computed on the device and every rank's moe_ep_dispatch writes its rows
+        straight into the owners' buffers: no schedule, no pull and no host
+        round trip (only the identity experts read the rows received back).
+        Returns the per-rank y, the counts and the rows each rank received."""
+        if fused_dispatch:
+            return self._step_fused(logits, xs, rep_off, rep_ids, recv_ex_out, stream)
         ev = self.plan_dispatch(logits, xs, rep_off, rep_ids, stream)
         counts = self.counts_host(ev)
         disp, comb, recv_rows = self.schedules(counts)
@@ -371,6 +420,24 @@ class EmulatedGroup:
         else:
             self.pull_combine(cu, cc, stream)
             ys = self.combine(T_list, stream=stream)
+        return ys, counts, recv_rows
+
+    def _step_fused(self, logits, xs, rep_off, rep_ids, recv_ex_out, stream):
+        self.plan_all(logits, rep_off, rep_ids, stream)
+        starts, rows_dev = self.starts_device(stream)
+        self.dispatch_fused(xs, starts, stream)
+        recv_rows = [int(v) for v in rows_dev.cpu().tolist()] if recv_ex_out is None else None
+        if recv_ex_out is None:
+            self.identity_experts(recv_rows, stream)
+        else:
+            for d in range(self.R):
+                self.recv_ex[d][:recv_ex_out[d].shape[0]].copy_(recv_ex_out[d])
+        cap = [t.shape[0] for t in self.recv_ex]
+        T_list = [lg.shape[0] for lg in logits]
+        ys = self.combine_fused(T_list, cap, starts, stream=stream)
+        counts = self.counts()
+        if recv_rows is None:
+            recv_rows = [int(v) for v in rows_dev.cpu().tolist()]
         return ys, counts, recv_rows
 
     def check(self) -> int:

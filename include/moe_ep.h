@@ -206,6 +206,42 @@ MOE_API int moe_ep_pull(const moe_ep_unit* units, const int32_t* core_off, int32
 MOE_API int moe_ep_recv_start(int32_t R, int32_t P, const int32_t* counts, int32_t s, int32_t* recv_start);
 
 /*
+ * moe_ep_recv_start on the device, for every rank at once, from the ranks'
+ * counts where the plans left them (no trip to the host):
+ *   counts      host array [R] of device addresses: rank q's int32 [P] counts
+ *   recv_start  device int32 [R, P]: row s is rank s's moe_ep_recv_start
+ *   recv_rows   device int32 [R]: rows each rank receives (may be NULL)
+ * (int32 tables of this header need 4-byte alignment only.)
+ * One launch of one CTA; it waits for the kernel before it (the plans) before
+ * reading the counts.
+ */
+MOE_API int moe_ep_recv_start_device(int32_t R, int32_t P, const int32_t* const* counts, int32_t* recv_start,
+                                     int32_t* recv_rows, void* stream);
+
+/*
+ * Fused dispatch of rank s (CloudMatrix384 write-up, "FusedDispatch and
+ * FusedCombine": each token quantized once and its rows written directly into
+ * the receivers' pre-allocated buffers, "AIV-Direct Write", in a token-level
+ * load -> quantize/address -> write pipeline).  Quantizes x as moe_dispatch
+ * does and writes copy (t, j) -- expert p = phys[t, j], owner floor(p R / P)
+ * -- to row recv_start[p] + slot[t, j] - offsets[p] of the owner's receive
+ * buffer, codes and scales, instead of the pool's own rows.  The receive
+ * buffers then hold exactly what moe_ep_pull (direction 0) would gather.
+ *   x            device bf16 [T, H] (read after the wait for the kernel before)
+ *   recv_codes   host array [R] of device addresses: each owner's int8 [rows, H]
+ *   recv_scales  host array [R] of device addresses: each owner's fp32
+ *                [rows, Gs] (Gs = the pool's scale stride, moe_view)
+ *   recv_rows    host int64 [R]: rows each owner's buffers hold (bounds)
+ *   recv_start   device int32 [P]: this rank's row of moe_ep_recv_start(_device),
+ *                4-byte aligned
+ * A row outside its owner's buffer is skipped and sets MOE_DEVERR_UNIT.
+ * Requires a prior moe_plan on this set with the same T.
+ */
+MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, int32_t R,
+                            int8_t* const* recv_codes, float* const* recv_scales, const int64_t* recv_rows,
+                            const int32_t* recv_start, void* stream);
+
+/*
  * Fused combine of rank s (a pull-mode reduction, StrataCL section 3.4:
  * remote operands loaded on chip and accumulated into the local output;
  * CloudMatrix384 write-up, "FusedDispatch and FusedCombine": expert output
@@ -220,7 +256,7 @@ MOE_API int moe_ep_recv_start(int32_t R, int32_t P, const int32_t* counts, int32
  *   recv_ex    host array [R] of device addresses: each owner's bf16 [rows, H]
  *              expert outputs (NULL with 0 rows for a rank that owns none)
  *   recv_rows  host int64 [R]: rows of each owner's buffer (bounds)
- *   recv_start device int32 [P] (moe_ep_recv_start of rank s)
+ *   recv_start device int32 [P] (moe_ep_recv_start of rank s), 4-byte aligned
  *   y          device bf16 [T, H]
  * A row outside its owner's buffer is skipped and sets MOE_DEVERR_UNIT in the
  * pool's error word.  Requires a prior moe_plan on this set with the same T.

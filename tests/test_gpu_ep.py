@@ -59,28 +59,33 @@ def _group(w, R, **kw):
     return ep.EmulatedGroup(R, max(w.T, 1), w.H, w.E, w.P, w.k, **kw)
 
 
-def _run(g, inps, recv_ex_out=None, fused=False):
+def _run(g, inps, recv_ex_out=None, fused=False, fused_dispatch=False):
     logits = [dev(i["logits"]) for i in inps]
     xs = [dev_bf16(i["x"]) for i in inps]
     ro = None if inps[0]["rep_off"] is None else dev(inps[0]["rep_off"])
     ri = None if inps[0]["rep_ids"] is None else dev(inps[0]["rep_ids"])
     rex = None if recv_ex_out is None else [dev_bf16(a) for a in recv_ex_out]
-    ys, counts, recv_rows = g.step(logits, xs, ro, ri, recv_ex_out=rex, fused_combine=fused)
+    ys, counts, recv_rows = g.step(logits, xs, ro, ri, recv_ex_out=rex, fused_combine=fused,
+                                   fused_dispatch=fused_dispatch)
     torch.cuda.synchronize()
     return ys, counts, recv_rows
 
 
-@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("mode", ["pull", "fused_combine", "fused"])
 @pytest.mark.parametrize("R,T,cores,cap,S", [(1, 96, 4, (8, 8), (64, 64)), (2, 150, 3, (1, 1), (5, 7)),
-                                             (3, 77, 8, (2, 1), (16, 3)), (4, 64, 16, (8, 8), (1, 1))])
-def test_split_small_identity_experts(R, T, cores, cap, S, fused):
+                                             (3, 77, 8, (2, 1), (16, 3)), (4, 64, 16, (8, 8), (1, 1)),
+                                             (5, 41, 2, (1, 1), (3, 3))])
+def test_split_small_identity_experts(R, T, cores, cap, S, mode):
     """The bench workload's experts (288 physical, 32 replicas) at small
-    batches: many small units, caps that bind, single-row units; the combine
-    either pulled back then reduced, or fused (rows read in place)."""
+    batches: many small units, caps that bind, single-row units; both
+    exchanges pulled, or the combine fused (rows read in place), or both
+    fused (rows written straight into the owners' buffers, window starts
+    computed on the device)."""
     w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T), H=1024)
     inps = _inputs(w, R)
     g = _group(w, R, cores=cores, desc_kw=dict(fanout_cap=cap, unit_rows=S))
-    ys, counts, recv_rows = _run(g, inps, fused=fused)
+    fused = mode != "pull"
+    ys, counts, recv_rows = _run(g, inps, fused=fused, fused_dispatch=mode == "fused")
     _check(g, inps, w, recv_rows, ys, counts, fused=fused)
 
 
@@ -100,6 +105,8 @@ def test_split_generated_expert_rows_and_ragged_batches():
     _check(g, inps, w, recv_rows, ys, counts, recv_ex_out=rex)
     ys, counts, recv_rows = _run(g, inps, rex, fused=True)
     _check(g, inps, w, recv_rows, ys, counts, recv_ex_out=rex, fused=True)
+    ys, counts, recv_rows = _run(g, inps, rex, fused=True, fused_dispatch=True)
+    _check(g, inps, w, recv_rows, ys, counts, recv_ex_out=rex, fused=True)
 
 
 def test_split_more_ranks_than_experts_and_one_hot_expert():
@@ -113,8 +120,8 @@ def test_split_more_ranks_than_experts_and_one_hot_expert():
         i["logits"][:, 1] = 4.0
         i["logits"][:, 2] = 3.0
     g = _group(w, R, cores=3)
-    for fused in (False, True):
-        ys, counts, recv_rows = _run(g, inps, fused=fused)
+    for fused, fd in ((False, False), (True, False), (True, True)):
+        ys, counts, recv_rows = _run(g, inps, fused=fused, fused_dispatch=fd)
         assert sorted(recv_rows) == [0, 0, 0, 0, R * w.T, R * w.T]
         _check(g, inps, w, recv_rows, ys, counts, fused=fused)
 
@@ -123,7 +130,9 @@ def test_split_full_bench_shape_eight_ranks():
     """Eight ranks of the bench workload (4096 tokens x 7168, 256 experts + 32
     replicas, top-8) with the default group cost model: every receive buffer,
     every returned row and every y compared in full; then the fused combine,
-    whose y must equal the pulled-back one bit for bit."""
+    and the fused dispatch with it (receive buffers filled with a pattern
+    first, so that every row must be written by it), whose y must equal the
+    pulled-back one bit for bit."""
     w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
     R = 8
     inps = _inputs(w, R)
@@ -133,10 +142,13 @@ def test_split_full_bench_shape_eight_ranks():
                             inps[0]["rep_ids"])
     _check(g, inps, w, recv_rows, ys, counts, ref=ref)
     ys_pulled = [y.clone() for y in ys]
-    ys, counts, recv_rows = _run(g, inps, fused=True)
-    _check(g, inps, w, recv_rows, ys, counts, ref=ref, fused=True)
-    for a, b in zip(ys, ys_pulled):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for fd in (False, True):
+        for t in g.recv_codes:  # the fused dispatch must write every row itself
+            t.fill_(0x55)
+        ys, counts, recv_rows = _run(g, inps, fused=True, fused_dispatch=fd)
+        _check(g, inps, w, recv_rows, ys, counts, ref=ref, fused=True)
+        for a, b in zip(ys, ys_pulled):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 def test_one_puller_per_launch_equals_all_pullers():
@@ -196,3 +208,19 @@ def test_fused_combine_rejects_rows_outside_the_owners_buffers():
     err = g.pools[0].check()
     assert err & ep.DEVERR_UNIT
     assert int((y.view(torch.int16) != 0).sum().item()) == 0
+
+
+def test_device_window_starts_equal_the_host_ones():
+    """moe_ep_recv_start_device against moe_ep_recv_start and the rows each
+    rank receives, at the bench shape and at a group with P < R."""
+    for w, R in ((wl.WORKLOADS["t4096_h7168_e256p288_k8"], 8), (wl.Workload("tiny", T=30, H=128, E=4, P=4, k=2), 6)):
+        w = wl.small_variant(w, min(w.T, 500))
+        inps = _inputs(w, R)
+        g = _group(w, R, cores=2)
+        g.plan_all([dev(i["logits"]) for i in inps], None if inps[0]["rep_off"] is None else dev(inps[0]["rep_off"]),
+                   None if inps[0]["rep_ids"] is None else dev(inps[0]["rep_ids"]))
+        starts, rows = g.starts_device()
+        counts = g.counts()
+        want = np.stack([ep.recv_start(counts, s) for s in range(R)])
+        np.testing.assert_array_equal(starts.cpu().numpy(), want)
+        np.testing.assert_array_equal(rows.cpu().numpy(), [int(ep.layout(counts, d)[0][-1]) for d in range(R)])
