@@ -747,6 +747,20 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
         return e0.elapsed_time(e1) / reps, 1e3 * statistics.median(sched_s) if sched_s else 0.0, out
 
     all_fused_ms, _, _ = timed_steps("all")
+    # the same fully fused step as one CUDA graph, replayed back to back
+    graph = g.fused_step_graph(logits, xs, ys, ro, ri)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    graph_ms = e0.elapsed_time(e1) / reps
+    del graph
     fused_ms, _, (fused_packed, _, _) = timed_steps(True)
     starts = fused_packed[4]
     step_ms, sched_ms, (packed, recv_rows, counts) = timed_steps(False)
@@ -787,7 +801,8 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
                      "what": "window starts on the device (moe_ep_recv_start_device), every rank's tokens "
                              "quantized and written straight into the owners' receive buffers "
                              "(moe_ep_dispatch), and the fused combine: no schedule, no pull, no host round "
-                             "trip"},
+                             "trip",
+                     "as_one_cuda_graph": {"value": R * w.T / (graph_ms * 1e-3), "ms_per_step": graph_ms}},
            "host_schedule_ms_per_step": sched_ms,
            "rows_exchanged": rows, "kernel_us_back_to_back": b2b,
            "pull_roofline": {k: {"bytes": moved[k], "achieved_gbs": moved[k] / (b2b[k] * 1e-6) / 1e9,

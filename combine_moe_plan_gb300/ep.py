@@ -286,6 +286,9 @@ class EmulatedGroup:
         self.recv_scales = [torch.empty((cap, self.Gs), dtype=torch.float32, device=device) for _ in range(R)]
         self.recv_ex = [torch.empty((cap, H), dtype=torch.bfloat16, device=device) for _ in range(R)]
         self.error_word = torch.zeros(1, dtype=torch.int32, device=device)
+        self._counts_host = torch.zeros((R, P), dtype=torch.int32).pin_memory()
+        self._starts = torch.empty((R, P), dtype=torch.int32, device=device)
+        self._rows = torch.empty(R, dtype=torch.int32, device=device)
         self.disp_planes = [plane([v["codes"] for v in self.views], self.recv_codes, H),
                             plane([v["scales"] for v in self.views], self.recv_scales, 4 * self.Gs)]
         self.comb_planes = [plane(self.recv_ex, [v["ex_out"] for v in self.views], 2 * H)]
@@ -298,8 +301,6 @@ class EmulatedGroup:
         s = stream or torch.cuda.current_stream(self.device)
         for pool, lg in zip(self.pools, logits):
             pool.plan(lg, rep_off, rep_ids, stream=s)
-        if not hasattr(self, "_counts_host"):
-            self._counts_host = torch.zeros((self.R, self.P), dtype=torch.int32).pin_memory()
         with torch.cuda.stream(s):
             for r, v in enumerate(self.views):
                 self._counts_host[r].copy_(v["counts"], non_blocking=True)
@@ -376,9 +377,6 @@ class EmulatedGroup:
     def starts_device(self, stream=None):
         """Every rank's window starts [R, P] and rows received [R], computed on
         the device from the plans' counts (moe_ep_recv_start_device)."""
-        if not hasattr(self, "_starts"):
-            self._starts = torch.empty((self.R, self.P), dtype=torch.int32, device=self.device)
-            self._rows = torch.empty(self.R, dtype=torch.int32, device=self.device)
         recv_start_device([v["counts"] for v in self.views], self._starts, self._rows, stream)
         return self._starts, self._rows
 
@@ -439,6 +437,30 @@ class EmulatedGroup:
         if recv_rows is None:
             recv_rows = [int(v) for v in rows_dev.cpu().tolist()]
         return ys, counts, recv_rows
+
+    def fused_step_graph(self, logits, xs, ys, rep_off=None, rep_ids=None, stream=None):
+        """The fully fused step (plans, device window starts, fused dispatch,
+        fused combine into ys) captured once as a CUDA graph: it reads no
+        counts on the host, so one replay runs the whole split.  The expert
+        outputs are whatever the receive buffers hold.  Replays read the
+        current contents of logits, xs and the replica map."""
+        s = stream or torch.cuda.Stream(device=self.device)
+        cap = [t.shape[0] for t in self.recv_ex]
+        T_list = [lg.shape[0] for lg in logits]
+
+        def body():
+            self.plan_all(logits, rep_off, rep_ids, s)
+            starts, _ = self.starts_device(s)
+            self.dispatch_fused(xs, starts, s)
+            self.combine_fused(T_list, cap, starts, ys=ys, stream=s)
+
+        with torch.cuda.stream(s):
+            body()  # warm (module loads, attributes) outside the capture
+        torch.cuda.synchronize(self.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        return g
 
     def check(self) -> int:
         """Synchronize; the pull error word OR every pool's error word."""

@@ -224,3 +224,64 @@ def test_device_window_starts_equal_the_host_ones():
         want = np.stack([ep.recv_start(counts, s) for s in range(R)])
         np.testing.assert_array_equal(starts.cpu().numpy(), want)
         np.testing.assert_array_equal(rows.cpu().numpy(), [int(ep.layout(counts, d)[0][-1]) for d in range(R)])
+
+
+def test_fused_split_as_one_cuda_graph():
+    """The fully fused step needs nothing from the host, so it is captured
+    once as a CUDA graph and replayed on new batches written into the same
+    input tensors: every replay's y against the oracle's split with the
+    expert outputs the receive buffers hold (seeded rows, fixed)."""
+    w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 200), H=512)
+    R = 4
+    g = _group(w, R, cores=8)
+    inps = _inputs(w, R, seed0=0)
+    logits = [dev(i["logits"]) for i in inps]
+    xs = [dev_bf16(i["x"]) for i in inps]
+    ro, ri = dev(inps[0]["rep_off"]), dev(inps[0]["rep_ids"])
+    ys = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    rng = np.random.default_rng(9)
+    fixed = [wl.f32_to_bf16_bits(rng.standard_normal((t.shape[0], w.H)).astype(np.float32)) for t in g.recv_ex]
+    for t, a in zip(g.recv_ex, fixed):
+        t.copy_(dev_bf16(a))
+    graph = g.fused_step_graph(logits, xs, ys, ro, ri)
+    for seed0 in (10, 20, 30):
+        new = _inputs(w, R, seed0=seed0)
+        for r in range(R):
+            logits[r].copy_(dev(new[r]["logits"]))
+            xs[r].copy_(dev_bf16(new[r]["x"]))
+        ro.copy_(dev(new[0]["rep_off"]))
+        ri.copy_(dev(new[0]["rep_ids"]))
+        for t, a in zip(g.recv_ex, fixed):  # the experts' outputs: the same rows in place every replay
+            t.copy_(dev_bf16(a))
+        graph.replay()
+        torch.cuda.synchronize()
+        counts = g.counts()
+        layouts = [ep.layout(counts, d) for d in range(R)]
+        rex = [fixed[d][:int(layouts[d][0][-1])] for d in range(R)]
+        ref = oracle.ep_forward([i["logits"] for i in new], [i["x"] for i in new], w.k, w.P, new[0]["rep_off"],
+                                new[0]["rep_ids"], recv_ex_out=rex)
+        for d in range(R):
+            n = int(layouts[d][0][-1])
+            np.testing.assert_array_equal(g.recv_codes[d][:n].cpu().numpy(), ref["recv_codes"][d])
+        for r in range(R):
+            assert_y_close(host_u16(ys[r]), ref["y"][r], f"replay {seed0} rank {r}")
+    assert g.check() == 0
+
+
+def test_fused_dispatch_rejects_rows_outside_the_owners_buffers():
+    """Window starts past an owner's rows: the fused dispatch skips those
+    copies, reports MOE_DEVERR_UNIT and writes nothing outside."""
+    w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 64), H=256)
+    R = 2
+    inps = _inputs(w, R)
+    g = _group(w, R, cores=2)
+    g.plan_all([dev(i["logits"]) for i in inps], dev(inps[0]["rep_off"]), dev(inps[0]["rep_ids"]))
+    starts, _ = g.starts_device()
+    starts[0].fill_(1 << 30)
+    for t in g.recv_codes:
+        t.zero_()
+    cap = [t.shape[0] for t in g.recv_codes]
+    ep.dispatch(g.pools[0], dev_bf16(inps[0]["x"]), g.recv_codes, g.recv_scales, cap, starts[0])
+    err = g.pools[0].check()
+    assert err & ep.DEVERR_UNIT
+    assert all(int(t.abs().sum().item()) == 0 for t in g.recv_codes)
