@@ -607,10 +607,12 @@ def run_ours(a, w: wl.Workload):
     decode = None if a.no_e2e else decode_latency(dev)
 
     # ---- phase E: the expert-parallel split, R ranks emulated on this GPU ----
-    split = None
+    split = split_decode = None
     if a.ep_ranks > 0 and ws == 1 and not a.no_e2e:
         torch.cuda.empty_cache()
         split = ep_split(dev, w, a.ep_ranks)
+        # the decode batch split the same way (one local batch of 96 tokens per rank)
+        split_decode = ep_split(dev, wl.WORKLOADS["t96_h7168_e256_k8"], a.ep_ranks, reps=100)
 
     # ---- max over ranks ----
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev)
@@ -669,6 +671,7 @@ def run_ours(a, w: wl.Workload):
             "clocks": clocks,
             "decode_latency": decode,
             "ep_split_emulated": split,
+            "ep_split_emulated_decode": split_decode,
         }
         if not a.no_cpu_baseline and ws == 1:
             out["cpu_baseline"] = cpu_baseline(w, inp)
