@@ -325,8 +325,7 @@ def _graph_per_op(torch, pool, logits, rep_off, rep_ids, x, y, T, reps=200, warm
     fused dispatch."""
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
-        pool.plan(logits, rep_off, rep_ids, buf=0, stream=s)
-        pool.dispatch(x, buf=0, stream=s, after_plan=True)
+        pool.plan_dispatch(logits, x, rep_off, rep_ids, buf=0, stream=s)
         pool.combine(T, y=y, buf=0, stream=s)
     torch.cuda.synchronize()
 
@@ -338,8 +337,7 @@ def _graph_per_op(torch, pool, logits, rep_off, rep_ids, x, y, T, reps=200, warm
 
     graphs = {
         "plan": capture(lambda: pool.plan(logits, rep_off, rep_ids, buf=0, stream=s)),
-        "plan+dispatch": capture(lambda: (pool.plan(logits, rep_off, rep_ids, buf=0, stream=s),
-                                     pool.dispatch(x, buf=0, stream=s, after_plan=True))),
+        "plan+dispatch": capture(lambda: pool.plan_dispatch(logits, x, rep_off, rep_ids, buf=0, stream=s)),
         "combine": capture(lambda: pool.combine(T, y=y, buf=0, stream=s)),
     }
     torch.cuda.synchronize()
@@ -370,26 +368,42 @@ def decode_latency(dev, reps=200):
     inp = wl.make_inputs(w)
     logits = torch.from_numpy(inp["logits"]).to(dev)
     x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
-    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=1, device=dev)
-    pool.view(0)["ex_out"][: w.rows].copy_(torch.from_numpy(inp["ex_out"].view(np.int16)).view(torch.bfloat16))
+    pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2, device=dev)
+    for b in range(2):
+        pool.view(b)["ex_out"][: w.rows].copy_(torch.from_numpy(inp["ex_out"].view(np.int16)).view(torch.bfloat16))
     y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
     s = torch.cuda.Stream(device=dev)
+    # Consecutive layers of one decode step: each layer its own router
+    # logits, its y the next layer's x, the two buffer sets alternating.
+    n_chain = 16
+    chain_logits = [torch.from_numpy(wl.make_inputs(w, seed=100 + l, with_expert_out=False)["logits"]).to(dev)
+                    for l in range(n_chain)]
+    chain_y = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(n_chain)]
+
+    def chain():
+        xin = x
+        for l in range(n_chain):
+            pool.plan_dispatch(chain_logits[l], xin, buf=l & 1, stream=s)
+            pool.combine(w.T, y=chain_y[l], buf=l & 1, stream=s)
+            xin = chain_y[l]
+
     with torch.cuda.stream(s):
         for _ in range(3):
-            pool.plan(logits, stream=s)
-            pool.dispatch(x, stream=s, after_plan=True)
+            pool.plan_dispatch(logits, x, stream=s)
             pool.combine(w.T, y=y, stream=s)
+        chain()
     torch.cuda.synchronize()
     g_disp, g_comb, g_layer = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_disp, stream=s):
-        pool.plan(logits, stream=s)
-        pool.dispatch(x, stream=s, after_plan=True)
+        pool.plan_dispatch(logits, x, stream=s)
     with torch.cuda.graph(g_comb, stream=s):
         pool.combine(w.T, y=y, stream=s)
     with torch.cuda.graph(g_layer, stream=s):
-        pool.plan(logits, stream=s)
-        pool.dispatch(x, stream=s, after_plan=True)
+        pool.plan_dispatch(logits, x, stream=s)
         pool.combine(w.T, y=y, stream=s)
+    g_chain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_chain, stream=s):
+        chain()
     torch.cuda.synchronize()
 
     def med(fn):
@@ -406,21 +420,24 @@ def decode_latency(dev, reps=200):
 
     pct = {"dispatch": med(g_disp.replay), "combine": med(g_comb.replay), "layer": med(g_layer.replay)}
 
-    def queued(fn, n=100):
+    def queued(fn, n=100, spin=40000):
         """GPU time of one replay whose launch the host has already queued: a
-        20 us spin kernel holds the stream while e0, the graph and e1 are
-        enqueued, so the interval excludes the host's launch latency."""
+        spin kernel (20 us by default) holds the stream while e0, the graph
+        and e1 are enqueued, so the interval excludes the host's launch
+        latency."""
         ts = []
         for _ in range(n):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            torch.cuda._sleep(40000)
+            torch.cuda._sleep(spin)
             e0.record()
             fn()
             e1.record()
             e1.synchronize()
             ts.append(e0.elapsed_time(e1))
-        return _percentiles_us(ts)
+        # Event timestamps here tick in steps of about 1 us, so the median
+        # sits on a step; the mean over the replays resolves finer.
+        return _percentiles_us(ts) + [float(np.mean(ts)) * 1e3]
 
     def back_to_back(fn, n=200):
         """Mean GPU time per replay over n replays queued back to back."""
@@ -436,6 +453,7 @@ def decode_latency(dev, reps=200):
         return e0.elapsed_time(e1) * 1e3 / n
 
     layer_q = queued(g_layer.replay)
+    chain_q = queued(g_chain.replay, n=50, spin=200000)
     # The floor of a graph of three kernels that do nothing (torch adds on 16
     # floats), queued the same way: what any three-kernel graph costs.
     tiny = torch.zeros(16, device=dev)
@@ -447,15 +465,22 @@ def decode_latency(dev, reps=200):
     empty_q = queued(g_empty.replay)
     out = {"workload": w.name, "dispatch_us": pct["dispatch"][1], "combine_us": pct["combine"][1],
            "layer_us": pct["layer"][1], "p10_p50_p90_us": pct,
-           "layer_queued_us": layer_q[1], "layer_queued_p10_p50_p90_us": layer_q,
+           "layer_queued_us": layer_q[1], "layer_queued_p10_p50_p90_us": layer_q[:3],
+           "layer_queued_mean_us": layer_q[3],
            "layer_back_to_back_us": back_to_back(g_layer.replay),
            "empty_three_kernel_graph_queued_us": empty_q[1],
+           "empty_three_kernel_graph_queued_mean_us": empty_q[3],
+           "layer_in_16_layer_graph_us": chain_q[3] / n_chain,
            "note": "CUDA-graph replays from an idle GPU; dispatch = plan + dispatch (the fused "
                    "dispatch carries the routing metadata); each graph launch adds its own overhead. "
                    "layer_queued: the same layer graph with its launch already queued behind a spin "
                    "kernel (the host's launch latency excluded); layer_back_to_back: mean per replay "
                    "of 200 replays queued back to back (consecutive layers); empty_three_kernel_graph: "
-                   "a graph of three do-nothing kernels queued the same way (the graph's own cost)"}
+                   "a graph of three do-nothing kernels queued the same way (the graph's own cost); "
+                   "layer_in_16_layer_graph: one replay of 16 consecutive layers (each its own logits, "
+                   "its y the next layer's x) captured as one graph and queued the same way, mean over 50 "
+                   "replays divided by 16. Event timestamps tick in steps of about 1 us: the medians sit "
+                   "on steps, the means resolve finer"}
     if pool.check() != 0:
         raise RuntimeError("device error word set in the decode-latency pass")
     return out
@@ -494,14 +519,14 @@ def run_ours(a, w: wl.Workload):
 
     def step(i, stream, ev=None):
         b = i & 1
-        if ev is not None:
+        if ev is None:
+            pool.plan_dispatch(logits, x, rep_off, rep_ids, buf=b, stream=stream)
+        else:  # the same two kernels with events between them
             ev[0].record(stream)
-        pool.plan(logits, rep_off, rep_ids, buf=b, stream=stream)
-        if ev is not None:
+            pool.plan(logits, rep_off, rep_ids, buf=b, stream=stream)
             ev[1].record(stream)
-        # the plan is the kernel just before and x is never written here
-        pool.dispatch(x, buf=b, stream=stream, after_plan=True)
-        if ev is not None:
+            # the plan is the kernel just before and x is never written here
+            pool.dispatch(x, buf=b, stream=stream, after_plan=True)
             ev[2].record(stream)
         pool.combine(w.T, y=ys[b], buf=b, stream=stream)
         if ev is not None:

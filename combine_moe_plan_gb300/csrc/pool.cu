@@ -271,6 +271,20 @@ MOE_API int moe_dispatch_after_plan(moe_pool* pool, const uint16_t* x, int32_t T
     return dispatch_call(pool, x, T, buf, true, stream);
 }
 
+MOE_API int moe_plan_dispatch(moe_pool* pool, const float* logits, int32_t T, const int32_t* rep_off,
+                              const int32_t* rep_ids, const uint16_t* x, int buf, void* stream) {
+    int rc = check_call(pool, T, buf);
+    if (rc != MOE_OK) return rc;
+    if (T > 0 && x == nullptr) return MOE_ERR_NULL;
+    if (T > 0 && !aligned16(x)) return MOE_ERR_ALIGN;
+    // The plan checks the rest before launching; with x checked first, an
+    // error leaves nothing enqueued.
+    if ((rc = moe_plan(pool, logits, T, rep_off, rep_ids, buf, stream)) != MOE_OK) return rc;
+    // The plan is the kernel just before, so the dispatch may load x while it
+    // runs: x was written before the plan in stream order.
+    return dispatch_call(pool, x, T, buf, true, stream);
+}
+
 MOE_API int moe_identity_experts(moe_pool* pool, int32_t T, int buf, void* stream) {
     int rc = check_call(pool, T, buf);
     if (rc != MOE_OK) return rc;
@@ -319,9 +333,7 @@ MOE_API int moe_step_host(moe_pool* pool, const float* h_logits, const uint16_t*
             cudaSuccess ||
         cudaMemcpyAsync(x, h_x, TH * sizeof(uint16_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if ((rc = moe_plan(pool, logits, T, rep_off, rep_ids, buf, stream)) != MOE_OK) return rc;
-    // The plan is the kernel just before, and x came in by a copy before it.
-    if ((rc = moe_dispatch_after_plan(pool, x, T, buf, stream)) != MOE_OK) return rc;
+    if ((rc = moe_plan_dispatch(pool, logits, T, rep_off, rep_ids, x, buf, stream)) != MOE_OK) return rc;
     if (h_ex_out != nullptr) {
         if (cudaMemcpyAsync(at<uint16_t>(pool, L.ex_out), h_ex_out, (size_t)T * d.k * d.H * sizeof(uint16_t),
                             cudaMemcpyHostToDevice, s) != cudaSuccess)

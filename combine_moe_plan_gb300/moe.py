@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         "moe_plan": [vp, vp, i32, vp, vp, ctypes.c_int, vp],
         "moe_dispatch": [vp, vp, i32, ctypes.c_int, vp],
         "moe_dispatch_after_plan": [vp, vp, i32, ctypes.c_int, vp],
+        "moe_plan_dispatch": [vp, vp, i32, vp, vp, vp, ctypes.c_int, vp],
         "moe_identity_experts": [vp, i32, ctypes.c_int, vp],
         "moe_combine": [vp, vp, vp, i32, ctypes.c_int, vp],
         "moe_step_host": [vp, vp, vp, vp, vp, i32, vp, vp, ctypes.c_int, vp],
@@ -196,6 +197,16 @@ class Pool:
         this set's plan on the same stream, with x written before that plan."""
         fn = "moe_dispatch_after_plan" if after_plan else "moe_dispatch"
         _call(fn, self.handle, _ptr(x), x.shape[0], buf, _stream(stream))
+
+    def plan_dispatch(self, logits, x, rep_off=None, rep_ids=None, buf=0, stream=None):
+        """moe_plan_dispatch: plan and dispatch as one call; the dispatch
+        reads x while the plan runs, which the call makes safe."""
+        T = logits.shape[0]
+        if x.shape[0] != T:
+            raise ValueError("logits and x must have the same number of tokens")
+        _call("moe_plan_dispatch", self.handle, _ptr(logits), T, _ptr(rep_off), _ptr(rep_ids), _ptr(x), buf,
+              _stream(stream))
+        return T
 
     def identity_experts(self, T, buf=0, stream=None):
         _call("moe_identity_experts", self.handle, T, buf, _stream(stream))

@@ -19,6 +19,8 @@
  *                 elements) and scatter of each token into its k slots
  *                 (write-up: "Early INT8 Quantization", "AIV-Direct Write",
  *                 "Token-Level Pipeline").
+ *   moe_plan_dispatch  both in one call; the dispatch then reads x while
+ *                 the plan runs, safely.
  *   (experts)     outside this library; moe_identity_experts is a stand-in
  *                 that dequantizes each slot row (code * scale -> bf16).
  *   moe_combine   gate-weighted gather-reduce of the k bf16 expert rows back
@@ -239,6 +241,21 @@ MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, 
 MOE_API int moe_dispatch_after_plan(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream);
 
 /*
+ * moe_plan_dispatch: moe_plan followed by moe_dispatch on set `buf` and
+ * `stream`, as one call (write-up, "FusedDispatch and FusedCombine": the
+ * routing metadata and the token data of one dispatch; "Token-Level
+ * Pipeline").  Arguments and errors as the two calls; x is checked before
+ * the plan is launched, so an error leaves nothing enqueued.  The results are
+ * the same bit for bit.  Because the plan is then the kernel just before the
+ * dispatch, the dispatch loads and quantizes x while the plan runs (as
+ * moe_dispatch_after_plan does), and that is always safe here: x and the
+ * logits may be written by anything earlier on `stream`, kernels included.
+ * T = 0: as moe_plan (x may be NULL).
+ */
+MOE_API int moe_plan_dispatch(moe_pool* pool, const float* logits, int32_t T, const int32_t* rep_off,
+                              const int32_t* rep_ids, const uint16_t* x, int buf, void* stream);
+
+/*
  * Identity experts (test stand-in for the expert FFNs): for rows r < T*k,
  * ex_out[r, i] = bf16(codes[r, i] * scales[r, i/128]).  Requires a prior
  * moe_plan and moe_dispatch on this set with the same T.
@@ -258,9 +275,9 @@ MOE_API int moe_combine(moe_pool* pool, const uint16_t* ex_out, uint16_t* y, int
 
 /*
  * One whole layer from HOST buffers: copy logits [T, E] and x [T, H] to the
- * device (into the set's staging area of the workspace), moe_plan (rep_off /
- * rep_ids are DEVICE pointers, as for moe_plan),
- * moe_dispatch, then either copy h_ex_out [T*k, H] (bf16 expert outputs, by
+ * device (into the set's staging area of the workspace), moe_plan_dispatch
+ * (rep_off / rep_ids are DEVICE pointers, as for moe_plan), then either copy
+ * h_ex_out [T*k, H] (bf16 expert outputs, by
  * row) into the set's ex_out buffer or, if h_ex_out is NULL, run
  * moe_identity_experts; then moe_combine and copy y [T, H] back to h_y.
  * All copies are cudaMemcpyAsync on `stream`; host buffers should be pinned.

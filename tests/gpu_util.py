@@ -66,7 +66,7 @@ def assert_y_close(y_gpu, y_ref, what=""):
 class Run:
     """One pass of the CUDA path over a workload's seeded inputs."""
 
-    def __init__(self, w, inp, T_max=None, n_sets=2, ex_out=None, buf=0, pool=None):
+    def __init__(self, w, inp, T_max=None, n_sets=2, ex_out=None, buf=0, pool=None, fused=False):
         self.w = w
         T = inp["logits"].shape[0]
         self.T = T
@@ -77,8 +77,11 @@ class Run:
         self.rep_ids = None if inp["rep_ids"] is None else dev(inp["rep_ids"])
         self.buf = buf
         p = self.pool
-        p.plan(self.logits, self.rep_off, self.rep_ids, buf=buf)
-        p.dispatch(self.x, buf=buf)
+        if fused:  # moe_plan_dispatch
+            p.plan_dispatch(self.logits, self.x, self.rep_off, self.rep_ids, buf=buf)
+        else:
+            p.plan(self.logits, self.rep_off, self.rep_ids, buf=buf)
+            p.dispatch(self.x, buf=buf)
         self.v = p.view(buf)
         if ex_out is None:
             p.identity_experts(T, buf=buf)

@@ -144,6 +144,26 @@ def test_dispatch_after_plan_checks_like_dispatch(L):
     L.moe_pool_destroy(h)
 
 
+def test_plan_dispatch_checks_like_plan_and_dispatch(L):
+    """moe_plan_dispatch rejects what moe_plan or moe_dispatch would reject,
+    before anything is launched (no GPU here: a call past the checks could
+    only fail with MOE_ERR_CUDA)."""
+    h, _ = _fake_pool(L)
+    good = ctypes.c_void_p(1 << 41)
+    odd = ctypes.c_void_p((1 << 41) + 4)
+    f = L.moe_plan_dispatch
+    assert f(h, good, -1, None, None, good, 0, None) == -2
+    assert f(h, good, 65, None, None, good, 0, None) == -2
+    assert f(h, good, 8, None, None, good, 2, None) == -4
+    assert f(h, None, 8, None, None, good, 0, None) == -1   # no logits
+    assert f(h, good, 8, None, None, None, 0, None) == -1   # no x
+    assert f(h, odd, 8, None, None, good, 0, None) == -3
+    assert f(h, good, 8, None, None, odd, 0, None) == -3
+    assert f(h, good, 8, good, None, good, 0, None) == -1   # half a replica map
+    assert f(None, good, 8, None, None, good, 0, None) == -1
+    L.moe_pool_destroy(h)
+
+
 @pytest.mark.parametrize("T", [0, 1, 96])
 def test_plan_static_checks_do_not_depend_on_T(L, T):
     """Every argument check of moe_plan_static runs before the empty-batch

@@ -4,7 +4,8 @@ ticket kernel instead, and larger ones with the three launches;
 MOE_PLAN_NO_CLUSTER=1 forces that.  The cluster plan's parity tests (every
 switch point from 1 to 513 tokens, graph capture, chained layers, the small
 workloads) are re-run in a child process with the variable set, so the same
-oracle comparisons cover the fallback."""
+oracle comparisons cover the fallback; so is the test file of
+moe_plan_dispatch."""
 import os
 import subprocess
 import sys
@@ -25,6 +26,16 @@ def test_cluster_parity_tests_pass_on_the_ticket_plan():
     r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_gpu_parity.py", "-k", sel, "-x", "-q",
                         "-m", "gpu", "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout
+
+
+def test_plan_dispatch_tests_pass_without_clusters():
+    """moe_plan_dispatch's whole test file, with the variable set."""
+    ensure_built()
+    env = dict(os.environ, MOE_PLAN_NO_CLUSTER="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_gpu_plan_dispatch.py", "-x", "-q", "-m", "gpu",
+                        "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
 

@@ -141,6 +141,20 @@ def _custom(T, H, E, P, k, logits, x=None, rep_off=None, rep_ids=None, seed=0, T
     return run
 
 
+# The three ways to run a batch's plan and dispatch: moe_plan + moe_dispatch
+# ("wait": x read after the wait), moe_plan + moe_dispatch_after_plan, and
+# moe_plan_dispatch (the two as one call).
+MODES = ["wait", "after_plan", "fused"]
+
+
+def _plan_dispatch(pool, mode, logits, ro, ri, x, buf, stream):
+    if mode == "fused":
+        pool.plan_dispatch(logits, x, ro, ri, buf=buf, stream=stream)
+    else:
+        pool.plan(logits, ro, ri, buf=buf, stream=stream)
+        pool.dispatch(x, buf=buf, stream=stream, after_plan=(mode == "after_plan"))
+
+
 def test_single_token():
     _custom(1, 256, 8, 8, 2, np.random.default_rng(1).standard_normal((1, 8)))
 
@@ -276,15 +290,14 @@ def test_launch_count():
     _check_all(big, inp, Run(big, inp, pool=pool))
 
 
-@pytest.mark.parametrize("after_plan", [False, True])
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("T", [40, 96, 200, 512, 1000])
-def test_step_captures_in_a_cuda_graph(T, after_plan):
+def test_step_captures_in_a_cuda_graph(T, mode):
     """plan -> dispatch -> combine (PDL launches) captured once in a CUDA graph
     and replayed on new input contents gives the oracle's results: 40, 96, 200
     and 512 tokens (cluster plans of 5 CTAs of 8 tokens, 6 of 16, 7 of 32 and
-    16 of 32) and 1000 (the three launches).  With after_plan the dispatch
-    waits on the cluster plan's per-tile flags, which every replay's plan
-    clears and sets again."""
+    16 of 32) and 1000 (the three launches), with plan and dispatch in each of
+    the three forms."""
     w = wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], T)
     pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
     inp0 = wl.make_inputs(w, seed=0)
@@ -293,14 +306,12 @@ def test_step_captures_in_a_cuda_graph(T, after_plan):
     y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):  # warm
-        pool.plan(logits, ro, ri, buf=1, stream=s)
-        pool.dispatch(x, buf=1, stream=s, after_plan=after_plan)
+        _plan_dispatch(pool, mode, logits, ro, ri, x, 1, s)
         pool.combine(w.T, y=y, ex_out=ex, buf=1, stream=s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        pool.plan(logits, ro, ri, buf=1, stream=s)
-        pool.dispatch(x, buf=1, stream=s, after_plan=after_plan)
+        _plan_dispatch(pool, mode, logits, ro, ri, x, 1, s)
         pool.combine(w.T, y=y, ex_out=ex, buf=1, stream=s)
     for seed in (3, 4, 5):
         inp = wl.make_inputs(w, seed=seed)
@@ -546,19 +557,18 @@ def test_bench_schedule_two_streams_full_size(after_plan):
         np.testing.assert_array_equal(v["codes"][:w.rows].cpu().numpy(), codes)
 
 
-@pytest.mark.parametrize("after_plan", [False, True])
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name,T", [("t96_h7168_e256_k8", 96), ("t4096_h7168_e256p288_k8", 300),
                                     ("t16384_h2048_e64_k6", 1000), ("t16384_h2048_e64_k6", 2000)])
-def test_layers_chained_on_one_stream(name, T, after_plan):
+def test_layers_chained_on_one_stream(name, T, mode):
     """Six layers back to back on one stream, each layer's y the next layer's x,
     the two buffer sets alternating, no synchronization in between; then the
     same chain captured once as a CUDA graph and replayed.  Every layer's y
     equals the oracle run layer after layer on its own outputs.  With
-    after_plan, dispatch reads x before its wait for the plan (and after a
-    cluster plan waits on per-tile flags, not the plan grid), so this checks
+    after_plan, dispatch reads x before its wait for the plan, so this checks
     that the previous layer's combine has finished writing x by then (the
-    plan in between waits for it) and that each layer's plan re-arms its
-    flags.
+    plan in between waits for it); moe_plan_dispatch does the same in one
+    call.
     The plan forms covered: cluster (96 tokens as 6 CTAs of 16, 300 as 10 of
     32) and three launches (1000 and 2000 tokens, 8-lane segments at 64
     experts); the test run without clusters adds the ticket kernel."""
@@ -583,8 +593,7 @@ def test_layers_chained_on_one_stream(name, T, after_plan):
         xin = x0
         for l in range(L):
             b = l & 1
-            pool.plan(lg[l], ro[l], ri[l], buf=b, stream=s)
-            pool.dispatch(xin, buf=b, stream=s, after_plan=after_plan)
+            _plan_dispatch(pool, mode, lg[l], ro[l], ri[l], xin, b, s)
             pool.identity_experts(w.T, buf=b, stream=s)
             pool.combine(w.T, y=ys[l], buf=b, stream=s)
             xin = ys[l]
