@@ -292,6 +292,7 @@ class EmulatedGroup:
         self.disp_planes = [plane([v["codes"] for v in self.views], self.recv_codes, H),
                             plane([v["scales"] for v in self.views], self.recv_scales, 4 * self.Gs)]
         self.comb_planes = [plane(self.recv_ex, [v["ex_out"] for v in self.views], 2 * H)]
+        self._plan_streams = None
 
     def plan_dispatch(self, logits, xs, rep_off=None, rep_ids=None, stream=None):
         """Every rank's plan, the counts on their way to the host, then every
@@ -299,8 +300,7 @@ class EmulatedGroup:
         in host memory (read them with counts_host()): the host can schedule
         while the dispatch kernels run."""
         s = stream or torch.cuda.current_stream(self.device)
-        for pool, lg in zip(self.pools, logits):
-            pool.plan(lg, rep_off, rep_ids, stream=s)
+        self.plan_all(logits, rep_off, rep_ids, s)
         with torch.cuda.stream(s):
             for r, v in enumerate(self.views):
                 self._counts_host[r].copy_(v["counts"], non_blocking=True)
@@ -371,8 +371,19 @@ class EmulatedGroup:
         return out
 
     def plan_all(self, logits, rep_off=None, rep_ids=None, stream=None):
-        for pool, lg in zip(self.pools, logits):
-            pool.plan(lg, rep_off, rep_ids, stream=stream)
+        """Every rank's plan.  The plans are independent and latency-bound, so
+        they run side by side on R streams forked from `stream` and joined
+        back to it (as the ranks of a real group plan at the same time)."""
+        s = stream or torch.cuda.current_stream(self.device)
+        if self._plan_streams is None:
+            self._plan_streams = [torch.cuda.Stream(device=self.device) for _ in range(self.R)]
+        fork = torch.cuda.Event()
+        fork.record(s)
+        for st, pool, lg in zip(self._plan_streams, self.pools, logits):
+            st.wait_event(fork)
+            pool.plan(lg, rep_off, rep_ids, stream=st)
+        for st in self._plan_streams:
+            s.wait_stream(st)
 
     def starts_device(self, stream=None):
         """Every rank's window starts [R, P] and rows received [R], computed on
