@@ -420,10 +420,11 @@ def decode_latency(dev, reps=200):
 
     pct = {"dispatch": med(g_disp.replay), "combine": med(g_comb.replay), "layer": med(g_layer.replay)}
 
-    def queued(fn, n=100, spin=40000):
+    def queued(fn, n=100, spin=100000):
         """GPU time of one replay whose launch the host has already queued: a
-        spin kernel (20 us by default) holds the stream while e0, the graph
-        and e1 are enqueued, so the interval excludes the host's launch
+        spin kernel (about 50 us by default; 20 us proved too short for the
+        host to enqueue e0, the graph and e1 every time) holds the stream
+        while they are enqueued, so the interval excludes the host's launch
         latency."""
         ts = []
         for _ in range(n):

@@ -292,7 +292,8 @@ class EmulatedGroup:
         self.disp_planes = [plane([v["codes"] for v in self.views], self.recv_codes, H),
                             plane([v["scales"] for v in self.views], self.recv_scales, 4 * self.Gs)]
         self.comb_planes = [plane(self.recv_ex, [v["ex_out"] for v in self.views], 2 * H)]
-        self._plan_streams = None
+        # one stream per rank for the plans (created here, never inside a capture)
+        self._plan_streams = [torch.cuda.Stream(device=self.device) for _ in range(R)]
 
     def plan_dispatch(self, logits, xs, rep_off=None, rep_ids=None, stream=None):
         """Every rank's plan, the counts on their way to the host, then every
@@ -375,8 +376,6 @@ class EmulatedGroup:
         they run side by side on R streams forked from `stream` and joined
         back to it (as the ranks of a real group plan at the same time)."""
         s = stream or torch.cuda.current_stream(self.device)
-        if self._plan_streams is None:
-            self._plan_streams = [torch.cuda.Stream(device=self.device) for _ in range(self.R)]
         fork = torch.cuda.Event()
         fork.record(s)
         for st, pool, lg in zip(self._plan_streams, self.pools, logits):
