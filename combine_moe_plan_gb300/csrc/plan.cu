@@ -393,20 +393,35 @@ plan_cluster_kernel(const float* __restrict__ logits, int T, int E, int P, int k
     const int tile = (int)cluster_ctarank();  // the grid is one cluster
     route_tile<EPL, kRouteInCluster, THREADS, TT>(logits, T, E, P, k, rep_off, rep_ids, topk_e, gates, phys,
                                                   nullptr, (int)gridDim.x, nullptr, err, smem, tile);
-    // route_tile's shared-memory layout: exp table, sel_v (here: the gates),
-    // sel_e, sel_p [TT k], masks [P], replica offsets [E+1] and ids [P]; then
-    // this kernel's arrays.
-    const float* sel_g = reinterpret_cast<const float*>(reinterpret_cast<float2*>(smem) + 2 * dword::kExpTableHalf + 1);
+    // route_tile's shared-memory layout: exp table, sel_v (the selected
+    // logits, then the gates), sel_e, sel_p [TT k], masks [P], replica
+    // offsets [E+1] and ids [P]; then this kernel's arrays.
+    const float2* s_exp = reinterpret_cast<const float2*>(smem);
+    float* sel_v = reinterpret_cast<float*>(reinterpret_cast<float2*>(smem) + 2 * dword::kExpTableHalf + 1);
+    const float* sel_g = sel_v;
     const int32_t* sel_e = reinterpret_cast<const int32_t*>(sel_g + TT * k);
     const int32_t* sel_p = sel_e + TT * k;
     const uint32_t* mask = reinterpret_cast<const uint32_t*>(sel_p + TT * k);
     int32_t* s_base = const_cast<int32_t*>(reinterpret_cast<const int32_t*>(mask + P)) + (E + 1) + P;  // [P]
     int32_t* offs = s_base + P;                                                                         // [P+1]
 
-    // Every tile's masks are complete and visible in the cluster.  route_tile
-    // left its global stores (top-k ids, gates, physical ids) to the placement
-    // loop below, so this barrier's release has only shared memory to publish.
-    cluster_sync();
+    // This CTA's masks are complete.  route_tile left its global stores
+    // (top-k ids, gates, physical ids) to the placement loop below, so this
+    // arrive's release has only shared memory to publish.
+    cluster_arrive();
+    // The gates, while the other CTAs arrive: the softmax over each token's
+    // selected logits (sel_v, read only by the warp of that token's items),
+    // kept in sel_v for the placement loop.
+    {
+        const float g = tile_gate<kRouteInCluster, TT>(T, k, tile * TT, sel_v, s_exp);
+        const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));
+        const int itl = (int)threadIdx.x / kp;
+        const int ij = (int)threadIdx.x - itl * kp;
+        __syncwarp();  // every lane of the token's segment has read sel_v
+        if (itl < TT && ij < k && tile * TT + itl < T) sel_v[itl * k + ij] = g;
+    }
+    // Every tile's masks are complete and visible in the cluster.
+    cluster_wait();
     MOE_TRACE_MARK(tr_single, 6);
 
     // Per physical expert: copies in earlier tiles and in all tiles.  Each

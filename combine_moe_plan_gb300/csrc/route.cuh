@@ -73,6 +73,71 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
+// The gate of this thread's item (token itl = threadIdx.x / kp of the tile,
+// j = threadIdx.x mod kp; 0 for a thread without an item), from the tile's
+// selected logits sel_v [TT k] and the exp table in shared memory.
+// Warp-collective in the first TT kp threads (whole warps).
+template <int WHERE, int TT>
+__device__ __forceinline__ float tile_gate(int T, int k, int t0, const float* sel_v, const float2* s_exp) {
+    // ---- gates: g_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), rounded once
+    // to fp32.  Each token's k items sit in one segment of kp lanes (kp the
+    // power of two >= k, so a segment never straddles a warp).  Each lane
+    // forms d = l_j - l_0 exactly as a pair of floats and e_j = exp(d) as a
+    // pair; a butterfly over the segment sums the pairs (every lane ends with
+    // the same s: the pair sum is commutative); each lane divides e_j by s and
+    // keeps the high float if Ziv's test shows it is the correctly rounded
+    // quotient.  A token with an item the pairs cannot decide, or with
+    // l_j - l_0 < -64, is redone in fp64 as e_j = exp(d) with e_0 = 1,
+    // s = sum over j ascending and g_j = (float)(e_j / s). ----
+    const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));  // TT kp <= the CTA's threads
+    const int itl = (int)threadIdx.x / kp;  // token within the tile (>= TT: no item)
+    const int ij = (int)threadIdx.x - itl * kp;
+    const int it = itl * k + ij;
+    const bool item_ok = itl < TT && ij < k && t0 + itl < T;
+    float g = 0.0f;
+    bool slow = false;
+    // Only the first TT kp threads hold items; warps past them skip the stage.
+    // The test is per warp (TT kp may be below 32), so a warp that enters
+    // enters whole and its full-mask shuffles see every lane.
+    const bool gate_warp = ((int)threadIdx.x & ~31) < TT * kp;
+    if (gate_warp) {
+        dword::dw e = {0.0f, 0.0f};
+        if (item_ok) {
+            const dword::dw d = dword::two_sum(sel_v[it], -sel_v[itl * k]);
+            if (d.h == 0.0f)
+                e = {1.0f, 0.0f};  // j == 0, or a tie with the top logit
+            else if (d.h >= -64.0f)
+                e = dword::exp_dw(d.h, d.l, s_exp);
+            else
+                slow = true;  // far below the top logit (or not finite)
+        }
+        dword::dw s = e;
+        for (int off = 1; off < kp; off <<= 1) {
+            const dword::dw o = {__shfl_xor_sync(kFull, s.h, off), __shfl_xor_sync(kFull, s.l, off)};
+            s = dword::dw_add(s, o);
+        }
+        if (item_ok && !slow) {
+            const dword::dw q = dword::dw_div(e, s);
+            g = q.h;
+            slow = !dword::rounds_safely(q);
+        }
+    }
+    ROUTE_MARK(2);
+    const unsigned slow_lanes = gate_warp ? __ballot_sync(kFull, slow) : 0u;
+    if (slow_lanes != 0u) {  // warp-uniform; rare
+        const int seg = (int)(threadIdx.x & 31) & ~(kp - 1);
+        const unsigned seg_bits = (kp == 32 ? 0xffffffffu : ((1u << kp) - 1u)) << seg;
+        const bool redo = (slow_lanes & seg_bits) != 0u && item_ok;
+        double e64 = 0.0;
+        if (redo) e64 = (ij == 0) ? 1.0 : exp((double)sel_v[it] - (double)sel_v[itl * k]);
+        double s64 = 0.0;
+        for (int jj = 0; jj < k; ++jj) s64 += __shfl_sync(kFull, e64, seg + jj);
+        if (redo) g = (float)(e64 / s64);
+    }
+    ROUTE_MARK(3);
+    return g;
+}
+
 // Route one tile of TT tokens (the body every plan kernel runs per CTA) with
 // a CTA of THREADS = TT L threads: each token's top-k runs on a segment of L
 // lanes (L = 32: a whole warp; 16 or 8 when the experts fit in at most 8 keys
@@ -188,62 +253,15 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     __syncthreads();
     ROUTE_MARK(1);
 
-    // ---- gates: g_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), rounded once
-    // to fp32.  Each token's k items sit in one segment of kp lanes (kp the
-    // power of two >= k, so a segment never straddles a warp).  Each lane
-    // forms d = l_j - l_0 exactly as a pair of floats and e_j = exp(d) as a
-    // pair; a butterfly over the segment sums the pairs (every lane ends with
-    // the same s: the pair sum is commutative); each lane divides e_j by s and
-    // keeps the high float if Ziv's test shows it is the correctly rounded
-    // quotient.  A token with an item the pairs cannot decide, or with
-    // l_j - l_0 < -64, is redone in fp64 as e_j = exp(d) with e_0 = 1,
-    // s = sum over j ascending and g_j = (float)(e_j / s). ----
     const int kp = k <= 1 ? 1 : 1 << (32 - __clz(k - 1));  // TT kp <= THREADS (host's choice of L)
     const int itl = (int)threadIdx.x / kp;  // token within the tile (>= 32: no item)
     const int ij = (int)threadIdx.x - itl * kp;
     const int it = itl * k + ij;
     const bool item_ok = itl < TT && ij < k && t0 + itl < T;
+    // The cluster plan computes the gates after its cluster barrier's arrive
+    // (tile_gate there), where they hide behind the wait for the other CTAs.
     float g = 0.0f;
-    bool slow = false;
-    // Only the first TT kp threads hold items; warps past them skip the stage.
-    // The test is per warp (TT kp may be below 32), so a warp that enters
-    // enters whole and its full-mask shuffles see every lane.
-    const bool gate_warp = ((int)threadIdx.x & ~31) < TT * kp;
-    if (gate_warp) {
-        dword::dw e = {0.0f, 0.0f};
-        if (item_ok) {
-            const dword::dw d = dword::two_sum(sel_v[it], -sel_v[itl * k]);
-            if (d.h == 0.0f)
-                e = {1.0f, 0.0f};  // j == 0, or a tie with the top logit
-            else if (d.h >= -64.0f)
-                e = dword::exp_dw(d.h, d.l, s_exp);
-            else
-                slow = true;  // far below the top logit (or not finite)
-        }
-        dword::dw s = e;
-        for (int off = 1; off < kp; off <<= 1) {
-            const dword::dw o = {__shfl_xor_sync(kFull, s.h, off), __shfl_xor_sync(kFull, s.l, off)};
-            s = dword::dw_add(s, o);
-        }
-        if (item_ok && !slow) {
-            const dword::dw q = dword::dw_div(e, s);
-            g = q.h;
-            slow = !dword::rounds_safely(q);
-        }
-    }
-    ROUTE_MARK(2);
-    const unsigned slow_lanes = gate_warp ? __ballot_sync(kFull, slow) : 0u;
-    if (slow_lanes != 0u) {  // warp-uniform; rare
-        const int seg = (int)(threadIdx.x & 31) & ~(kp - 1);
-        const unsigned seg_bits = (kp == 32 ? 0xffffffffu : ((1u << kp) - 1u)) << seg;
-        const bool redo = (slow_lanes & seg_bits) != 0u && item_ok;
-        double e64 = 0.0;
-        if (redo) e64 = (ij == 0) ? 1.0 : exp((double)sel_v[it] - (double)sel_v[itl * k]);
-        double s64 = 0.0;
-        for (int jj = 0; jj < k; ++jj) s64 += __shfl_sync(kFull, e64, seg + jj);
-        if (redo) g = (float)(e64 / s64);
-    }
-    ROUTE_MARK(3);
+    if (WHERE != kRouteInCluster) g = tile_gate<WHERE, TT>(T, k, t0, sel_v, s_exp);
     if (item_ok) {
         const int tt = t0 + itl;
         const int e = sel_e[it];
@@ -274,9 +292,6 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     }
     __syncthreads();
     ROUTE_MARK(4);
-    // In the cluster plan the gate goes to shared memory (sel_v is not read
-    // after the barrier above) for the stores after the cluster barrier.
-    if (WHERE == kRouteInCluster && item_ok) sel_v[it] = g;
 
     // ---- tile histogram (expert-major) and in-tile ranks ----
     if (WHERE != kRouteInCluster) {

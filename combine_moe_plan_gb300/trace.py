@@ -68,18 +68,22 @@ def read(kind: int):
 
 def summarize(kind: int, n_ctas: int) -> dict:
     """Per-stage durations (ns) across the first n_ctas CTAs of the last launch
-    of `kind`: median and 90th percentile of (stamp[s] - stamp[s-1]) over CTAs
-    that reached stage s, plus the launch span and the SMs used."""
+    of `kind`: median and 90th percentile of (stamp[b] - stamp[a]) over CTAs
+    that reached both, for consecutive stages a, b in the order they were
+    reached (by median stamp: the cluster plan computes its gates, stages 2
+    and 3, after stage 5), plus the launch span and the SMs used."""
     name, stages = KINDS[kind]
     st, sm = read(kind)
     ns = st[:n_ctas, :, 0].astype(np.int64)
     ran = ns[:, 0] > 0  # the stamps are cleared before each pass
     out = {"kernel": name, "ctas": int(ran.sum()), "sms": int(len(np.unique(sm[:n_ctas][ran]))), "stages": {}}
-    for s in range(1, len(stages)):
-        ok = (ns[:, s] > 0) & (ns[:, s - 1] > 0)
+    seen = [s for s in range(len(stages)) if (ns[:, s] > 0).any()]
+    order = sorted(seen, key=lambda s: (float(np.median(ns[ns[:, s] > 0, s])), s))
+    for a, b in zip(order[:-1], order[1:]):
+        ok = (ns[:, b] > 0) & (ns[:, a] > 0)
         if ok.any():
-            d = ns[ok, s] - ns[ok, s - 1]
-            out["stages"][f"{stages[s - 1]}->{stages[s]}"] = {
+            d = ns[ok, b] - ns[ok, a]
+            out["stages"][f"{stages[a]}->{stages[b]}"] = {
                 "median_ns": float(np.median(d)), "p90_ns": float(np.percentile(d, 90)), "ctas": int(ok.sum())}
     started = ns[:, 0][ns[:, 0] > 0]
     last = ns.max(axis=1)
