@@ -292,8 +292,23 @@ class EmulatedGroup:
         self.disp_planes = [plane([v["codes"] for v in self.views], self.recv_codes, H),
                             plane([v["scales"] for v in self.views], self.recv_scales, 4 * self.Gs)]
         self.comb_planes = [plane(self.recv_ex, [v["ex_out"] for v in self.views], 2 * H)]
-        # one stream per rank for the plans (created here, never inside a capture)
-        self._plan_streams = [torch.cuda.Stream(device=self.device) for _ in range(R)]
+        # one stream per rank (created here, never inside a capture)
+        self._rank_streams = [torch.cuda.Stream(device=self.device) for _ in range(R)]
+
+    def _per_rank(self, stream, fn):
+        """fn(r, s_r) for every rank r, each on its own stream s_r forked from
+        `stream` and joined back to it: the emulated ranks' kernels run side
+        by side, as the ranks of a real group do on their own GPUs."""
+        s = stream or torch.cuda.current_stream(self.device)
+        fork = torch.cuda.Event()
+        fork.record(s)
+        out = []
+        for r, st in enumerate(self._rank_streams):
+            st.wait_event(fork)
+            out.append(fn(r, st))
+        for st in self._rank_streams:
+            s.wait_stream(st)
+        return out
 
     def plan_dispatch(self, logits, xs, rep_off=None, rep_ids=None, stream=None):
         """Every rank's plan, the counts on their way to the host, then every
@@ -307,8 +322,8 @@ class EmulatedGroup:
                 self._counts_host[r].copy_(v["counts"], non_blocking=True)
         ev = torch.cuda.Event()
         ev.record(s)
-        for pool, x in zip(self.pools, xs):
-            pool.dispatch(x, stream=s)  # the kernel before it is not its own plan: the default form
+        # the kernel before each dispatch is not its own plan: the default form
+        self._per_rank(s, lambda r, st: self.pools[r].dispatch(xs[r], stream=st))
         return ev
 
     def counts_host(self, ev) -> np.ndarray:
@@ -346,13 +361,21 @@ class EmulatedGroup:
         pull(units, core_off, self.R, self.cores, 0, self.R, self.comb_planes, self.error_word, stream)
 
     def identity_experts(self, recv_rows, stream=None):
-        for d in range(self.R):
+        def one(d, st):
             if recv_rows[d]:
-                dequant_rows(self.recv_codes[d], self.recv_scales[d], recv_rows[d], self.recv_ex[d], stream)
+                dequant_rows(self.recv_codes[d], self.recv_scales[d], recv_rows[d], self.recv_ex[d], st)
+        self._per_rank(stream, one)
+
+    def _outputs(self, T_list, stream):
+        """Every rank's y [T, H], allocated on `stream` (the one they are
+        handed back on)."""
+        with torch.cuda.stream(stream or torch.cuda.current_stream(self.device)):
+            return [torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device) for T in T_list]
 
     def combine(self, T_list, ys=None, stream=None):
-        return [pool.combine(T, y=None if ys is None else ys[r], stream=stream)
-                for r, (pool, T) in enumerate(zip(self.pools, T_list))]
+        ys = ys or self._outputs(T_list, stream)
+        self._per_rank(stream, lambda r, st: self.pools[r].combine(T_list[r], y=ys[r], stream=st))
+        return ys
 
     def recv_starts(self, counts, stream=None):
         """Every rank's recv_start table [R, P] on the device (copied on `stream`)."""
@@ -364,25 +387,16 @@ class EmulatedGroup:
     def combine_fused(self, T_list, recv_rows, starts, ys=None, stream=None):
         """Every rank's y straight from the owners' receive buffers (no
         combine pull): moe_ep_combine per rank."""
-        out = []
-        for r, (pool, T) in enumerate(zip(self.pools, T_list)):
-            y = ys[r] if ys is not None else torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device)
-            combine(pool, T, self.recv_ex, recv_rows, starts[r], y, stream=stream)
-            out.append(y)
-        return out
+        ys = ys or self._outputs(T_list, stream)
+        self._per_rank(stream, lambda r, st: combine(self.pools[r], T_list[r], self.recv_ex, recv_rows, starts[r],
+                                                      ys[r], stream=st))
+        return ys
 
     def plan_all(self, logits, rep_off=None, rep_ids=None, stream=None):
         """Every rank's plan.  The plans are independent and latency-bound, so
         they run side by side on R streams forked from `stream` and joined
         back to it (as the ranks of a real group plan at the same time)."""
-        s = stream or torch.cuda.current_stream(self.device)
-        fork = torch.cuda.Event()
-        fork.record(s)
-        for st, pool, lg in zip(self._plan_streams, self.pools, logits):
-            st.wait_event(fork)
-            pool.plan(lg, rep_off, rep_ids, stream=st)
-        for st in self._plan_streams:
-            s.wait_stream(st)
+        self._per_rank(stream, lambda r, st: self.pools[r].plan(logits[r], rep_off, rep_ids, stream=st))
 
     def starts_device(self, stream=None):
         """Every rank's window starts [R, P] and rows received [R], computed on
@@ -393,8 +407,8 @@ class EmulatedGroup:
     def dispatch_fused(self, xs, starts, stream=None):
         """Every rank's fused dispatch into the owners' receive buffers."""
         cap = [t.shape[0] for t in self.recv_codes]
-        for r, (pool, x) in enumerate(zip(self.pools, xs)):
-            dispatch(pool, x, self.recv_codes, self.recv_scales, cap, starts[r], stream=stream)
+        self._per_rank(stream, lambda r, st: dispatch(self.pools[r], xs[r], self.recv_codes, self.recv_scales, cap,
+                                                       starts[r], stream=st))
 
     def step(self, logits, xs, rep_off=None, rep_ids=None, recv_ex_out=None, stream=None, fused_combine=False,
              fused_dispatch=False):

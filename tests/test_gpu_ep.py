@@ -89,6 +89,20 @@ def test_split_small_identity_experts(R, T, cores, cap, S, mode):
     _check(g, inps, w, recv_rows, ys, counts, fused=fused)
 
 
+@pytest.mark.parametrize("mode", ["pull", "fused"])
+def test_split_at_the_largest_group(mode):
+    """MOE_EP_MAX_RANKS = 64 ranks of 16 tokens over the bench workload's 288
+    physical experts (four or five experts a rank; the pointer tables, the
+    device window starts over 64 x 288 counts and the schedules at their
+    largest group)."""
+    R = 64
+    w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 16), H=256)
+    inps = _inputs(w, R)
+    g = _group(w, R)
+    ys, counts, recv_rows = _run(g, inps, fused=mode == "fused", fused_dispatch=mode == "fused")
+    _check(g, inps, w, recv_rows, ys, counts, fused=mode == "fused")
+
+
 def test_split_generated_expert_rows_and_ragged_batches():
     """Receivers' expert outputs are seeded bf16 rows; the ranks' batches
     differ in size, one rank's batch is empty."""
