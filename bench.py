@@ -743,7 +743,7 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
             g.plan_all(logits, ro, ri)
             starts_dev, _ = g.starts_device()
             g.dispatch_fused(xs, starts_dev)
-            g.combine_fused([w.T] * R, cap, starts_dev, ys=ys)
+            g.combine_fused([w.T] * R, cap, starts_dev, ys=ys, recorded=True)
             return None
         ev = g.plan_dispatch(logits, xs, ro, ri)
         counts = g.counts_host(ev)
@@ -799,8 +799,11 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
     b2b = {}
     for name, fn in (("dispatch_pull", lambda: g.pull_dispatch(du, dc)),
                      ("combine_pull", lambda: g.pull_combine(cu, cc)),
-                     ("fused_combine_all_ranks", lambda: g.combine_fused([w.T] * R, recv_rows, starts, ys=ys)),
-                     ("fused_dispatch_all_ranks", lambda: g.dispatch_fused(xs, starts_dev))):
+                     ("fused_dispatch_all_ranks", lambda: g.dispatch_fused(xs, starts_dev)),
+                     ("fused_combine_all_ranks", lambda: g.combine_fused([w.T] * R, cap, starts_dev, ys=ys,
+                                                                         recorded=True)),
+                     ("fused_combine_rows_found_all_ranks",
+                      lambda: g.combine_fused([w.T] * R, recv_rows, starts, ys=ys))):
         for _ in range(3):
             fn()
         a0 = torch.cuda.Event(enable_timing=True)
@@ -816,6 +819,7 @@ def ep_split(dev, w, R, reps=20, n_b2b=20, unit_rows=0):
     rows = int(sum(recv_rows))
     moved = {"dispatch_pull": 2 * rows * (w.H + 4 * g.Gs), "combine_pull": 2 * rows * 2 * w.H,
              "fused_combine_all_ranks": R * w.algorithmic_bytes()["combine"],
+             "fused_combine_rows_found_all_ranks": R * w.algorithmic_bytes()["combine"],
              "fused_dispatch_all_ranks": R * w.algorithmic_bytes()["dispatch"]}
     peak, peak_src = _peaks()
     out = {"ranks": R, "workload_per_rank": w.name, "cores_per_puller": g.cores,

@@ -378,6 +378,7 @@ void schedule_one(const moe_ep_desc& desc, const Windows& w, const int32_t* coun
 // ------------------------------------------------------- fused combine ----
 
 constexpr int kCombineThreads = 256;  // 8 warps; one warp per (token, 256 elements)
+constexpr int kRowBits = 40;          // a recorded copy row: owner * 2^40 + row
 constexpr int kCombineSeg = 256;      // 32 lanes x 8 bf16 (16 bytes a lane)
 
 struct RecvTable {
@@ -388,12 +389,12 @@ struct RecvTable {
 // Lane j < k of a warp holds copy j of token t: its owner's row address and
 // gate.  KB copies' 16-byte loads are in flight per lane before they are
 // accumulated in ascending j, as in the single-GPU combine.
-template <int KB>
+template <int KB, bool RECORDED>  // RECORDED: copy_row holds each copy's row
 __global__ void __launch_bounds__(kCombineThreads)
 ep_combine_kernel(const int32_t* __restrict__ slot, const float* __restrict__ gates,
                   const int32_t* __restrict__ phys, const int32_t* __restrict__ offsets,
-                  const int32_t* __restrict__ recv_start, int T, int H, int k, int R, int P, const RecvTable tab,
-                  uint16_t* __restrict__ y, int32_t* __restrict__ err) {
+                  const int32_t* __restrict__ recv_start, const int64_t* __restrict__ copy_row, int T, int H, int k,
+                  int R, int P, const RecvTable tab, uint16_t* __restrict__ y, int32_t* __restrict__ err) {
     grid_dependency_sync();
     const int lane = threadIdx.x & 31;
     const int segs = (H + kCombineSeg - 1) / kCombineSeg;
@@ -406,19 +407,27 @@ ep_combine_kernel(const int32_t* __restrict__ slot, const float* __restrict__ ga
     float g = 0.0f;
     bool bad = false;
     if (lane < k) {
-        const int r = slot[(size_t)t * k + lane];
-        const int p = phys[(size_t)t * k + lane];
         g = gates[(size_t)t * k + lane];
-        if (p < 0 || p >= P) {
-            bad = true;
+        int d = -1;
+        long long row = -1;
+        if (RECORDED) {  // recorded by the fused dispatch: one load
+            const long long v = copy_row[(size_t)t * k + lane];
+            if (v >= 0) {
+                d = (int)(v >> kRowBits);
+                row = v & ((1LL << kRowBits) - 1);
+            }
         } else {
-            const int d = (int)(((long long)p * R) / P);
-            const long long row = (long long)recv_start[p] + r - offsets[p];
-            if (row < 0 || row >= tab.rows[d] || tab.ex[d] == nullptr)
-                bad = true;
-            else
-                src = reinterpret_cast<unsigned long long>(tab.ex[d] + row * H);
+            const int r = slot[(size_t)t * k + lane];
+            const int p = phys[(size_t)t * k + lane];
+            if (p >= 0 && p < P) {
+                d = (int)(((long long)p * R) / P);
+                row = (long long)recv_start[p] + r - offsets[p];
+            }
         }
+        if (d < 0 || d >= R || row < 0 || row >= tab.rows[d] || tab.ex[d] == nullptr)
+            bad = true;
+        else
+            src = reinterpret_cast<unsigned long long>(tab.ex[d] + row * H);
     }
     if (__any_sync(kFull, bad)) {  // warp-uniform: skip the token's segment
         if (lane == 0) set_error(err, MOE_DEVERR_UNIT);
@@ -551,7 +560,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
 ep_dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, int R, int P, int Gs,
                    const int32_t* __restrict__ slot, const int32_t* __restrict__ phys,
                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ recv_start, const SendTable tab,
-                   int32_t* __restrict__ err) {
+                   int64_t* __restrict__ copy_row, int32_t* __restrict__ err) {
     grid_dependency_sync();
     allow_dependents();
     const int lane = threadIdx.x & 31;
@@ -572,12 +581,16 @@ ep_dispatch_kernel(const uint16_t* __restrict__ x, int T, int H, int k, int R, i
             d = (int)(((long long)p * R) / P);
             row = (long long)recv_start[p] + r - offsets[p];
         }
-        if (row < 0 || row >= tab.rows[d] || tab.codes[d] == nullptr || tab.scales[d] == nullptr) {
+        const bool ok = row >= 0 && row < tab.rows[d] && tab.codes[d] != nullptr && tab.scales[d] != nullptr;
+        if (!ok) {
             set_error(err, MOE_DEVERR_UNIT);
         } else {
             cdst = reinterpret_cast<unsigned long long>(tab.codes[d] + row * H);
             sdst = tab.scales[d] + row * Gs;
         }
+        // where the copy went, once per copy (by the warp of segment 0)
+        if (copy_row != nullptr && seg == 0)
+            copy_row[(size_t)t * k + lane] = ok ? ((long long)d << kRowBits) | row : -1LL;
     }
     const SegQuant qz = quantize_segment(ld);
     for (int j = 0; j < k; ++j) {
@@ -779,7 +792,7 @@ MOE_API int moe_ep_recv_start_device(int32_t R, int32_t P, const int32_t* const*
 
 MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, int32_t R,
                             int8_t* const* recv_codes, float* const* recv_scales, const int64_t* recv_rows,
-                            const int32_t* recv_start, void* stream) {
+                            const int32_t* recv_start, int64_t* copy_row, void* stream) {
     if (pool == nullptr || recv_codes == nullptr || recv_scales == nullptr || recv_rows == nullptr)
         return MOE_ERR_NULL;
     const moe_desc& d = pool->geo.d;
@@ -789,7 +802,9 @@ MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int bu
     if (T == 0) return MOE_OK;
     if (x == nullptr || recv_start == nullptr) return MOE_ERR_NULL;
     auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
-    if (misaligned(x) || (reinterpret_cast<uintptr_t>(recv_start) & 3u) != 0) return MOE_ERR_ALIGN;
+    if (misaligned(x) || (reinterpret_cast<uintptr_t>(recv_start) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(copy_row) & 7u) != 0)
+        return MOE_ERR_ALIGN;
     SendTable tab;
     std::memset(&tab, 0, sizeof(tab));
     for (int q = 0; q < R; ++q) {
@@ -798,6 +813,7 @@ MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int bu
         tab.codes[q] = recv_codes[q];
         tab.scales[q] = recv_scales[q];
         tab.rows[q] = (recv_codes[q] == nullptr || recv_scales[q] == nullptr) ? 0 : recv_rows[q];
+        if (tab.rows[q] >= (1LL << kRowBits)) return MOE_ERR_SIZE;
     }
     const SetLayout& L = pool->geo.set[buf];
     char* base = pool->base;
@@ -806,7 +822,7 @@ MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int bu
     cudaError_t e = launch_pdl(ep_dispatch_kernel, grid, dim3(kDispatchThreads), 0, static_cast<cudaStream_t>(stream),
                                x, T, d.H, d.k, R, d.P, pool->geo.Gs, reinterpret_cast<const int32_t*>(base + L.slot),
                                reinterpret_cast<const int32_t*>(base + L.phys),
-                               reinterpret_cast<const int32_t*>(base + L.offsets), recv_start, tab,
+                               reinterpret_cast<const int32_t*>(base + L.offsets), recv_start, tab, copy_row,
                                reinterpret_cast<int32_t*>(base + pool->geo.error_word));
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     pool->launches += 1;
@@ -814,16 +830,19 @@ MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int bu
 }
 
 MOE_API int moe_ep_combine(moe_pool* pool, int32_t T, int buf, int32_t R, const uint16_t* const* recv_ex,
-                           const int64_t* recv_rows, const int32_t* recv_start, uint16_t* y, void* stream) {
+                           const int64_t* recv_rows, const int32_t* recv_start, const int64_t* copy_row,
+                           uint16_t* y, void* stream) {
     if (pool == nullptr || recv_ex == nullptr || recv_rows == nullptr) return MOE_ERR_NULL;
     const moe_desc& d = pool->geo.d;
     if (buf < 0 || buf >= d.n_sets) return MOE_ERR_BUF;
     if (T < 0 || T > d.T_max || R < 1 || R > MOE_EP_MAX_RANKS) return MOE_ERR_SIZE;
     if (pool->planned_T[buf] != T) return MOE_ERR_STATE;
     if (T == 0) return MOE_OK;
-    if (recv_start == nullptr || y == nullptr) return MOE_ERR_NULL;
+    if ((recv_start == nullptr && copy_row == nullptr) || y == nullptr) return MOE_ERR_NULL;
     auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
-    if ((reinterpret_cast<uintptr_t>(recv_start) & 3u) != 0 || misaligned(y)) return MOE_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(recv_start) & 3u) != 0 || (reinterpret_cast<uintptr_t>(copy_row) & 7u) != 0 ||
+        misaligned(y))
+        return MOE_ERR_ALIGN;
     RecvTable tab;
     std::memset(&tab, 0, sizeof(tab));
     for (int q = 0; q < R; ++q) {
@@ -844,8 +863,11 @@ MOE_API int moe_ep_combine(moe_pool* pool, int32_t T, int buf, int32_t R, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
 #define MOE_EP_COMBINE_CASE(KB)                                                                              \
-    e = launch_pdl(ep_combine_kernel<KB>, grid, dim3(kCombineThreads), 0, s, slot, gates, phys, offsets,      \
-                   recv_start, T, d.H, d.k, R, d.P, tab, y, err)
+    e = copy_row != nullptr                                                                                   \
+            ? launch_pdl(ep_combine_kernel<KB, true>, grid, dim3(kCombineThreads), 0, s, slot, gates, phys,   \
+                         offsets, recv_start, copy_row, T, d.H, d.k, R, d.P, tab, y, err)                     \
+            : launch_pdl(ep_combine_kernel<KB, false>, grid, dim3(kCombineThreads), 0, s, slot, gates, phys,  \
+                         offsets, recv_start, copy_row, T, d.H, d.k, R, d.P, tab, y, err)
     switch (d.k < 8 ? d.k : 8) {
         case 1: MOE_EP_COMBINE_CASE(1); break;
         case 2: MOE_EP_COMBINE_CASE(2); break;

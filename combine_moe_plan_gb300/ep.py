@@ -60,8 +60,8 @@ def lib():
             "moe_dequant_rows": [vp, vp, i32, i32, i32, vp, vp],
             "moe_ep_recv_start": [i32, i32, vp, i32, vp],
             "moe_ep_recv_start_device": [i32, i32, pp(vp), vp, vp, vp],
-            "moe_ep_dispatch": [vp, vp, i32, ctypes.c_int, i32, pp(vp), pp(vp), pp(i64), vp, vp],
-            "moe_ep_combine": [vp, i32, ctypes.c_int, i32, pp(vp), pp(i64), vp, vp, vp],
+            "moe_ep_dispatch": [vp, vp, i32, ctypes.c_int, i32, pp(vp), pp(vp), pp(i64), vp, vp, vp],
+            "moe_ep_combine": [vp, i32, ctypes.c_int, i32, pp(vp), pp(i64), vp, vp, vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -192,25 +192,29 @@ def recv_start_device(counts_dev, recv_start_dev, recv_rows_dev=None, stream=Non
           None if recv_rows_dev is None else recv_rows_dev.data_ptr(), moe._stream(stream))
 
 
-def dispatch(pool, x, recv_codes, recv_scales, recv_rows, recv_start_dev, buf=0, stream=None):
+def dispatch(pool, x, recv_codes, recv_scales, recv_rows, recv_start_dev, buf=0, stream=None, copy_row=None):
     """moe_ep_dispatch: the rank's tokens quantized and written straight into
-    the owners' receive buffers."""
+    the owners' receive buffers; with copy_row (device int64 [T, k]) where
+    each copy went is recorded for moe_ep_combine."""
     R = len(recv_codes)
     cp = (vp * R)(*[None if t is None else t.data_ptr() for t in recv_codes])
     sp = (vp * R)(*[None if t is None else t.data_ptr() for t in recv_scales])
     rows = (i64 * R)(*[int(r) for r in recv_rows])
     _call("moe_ep_dispatch", pool.handle, x.data_ptr() if x.numel() else None, x.shape[0], buf, R, cp, sp, rows,
-          recv_start_dev.data_ptr(), moe._stream(stream))
+          recv_start_dev.data_ptr(), None if copy_row is None else copy_row.data_ptr(), moe._stream(stream))
 
 
-def combine(pool, T, recv_ex, recv_rows, recv_start_dev, y, buf=0, stream=None):
+def combine(pool, T, recv_ex, recv_rows, recv_start_dev, y, buf=0, stream=None, copy_row=None):
     """moe_ep_combine: rank's y [T, H] straight from the owners' receive buffers
-    (recv_ex: per-rank bf16 device tensors, recv_rows: rows each holds)."""
+    (recv_ex: per-rank bf16 device tensors, recv_rows: rows each holds); with
+    copy_row, the rows its moe_ep_dispatch recorded (recv_start_dev may then be
+    None)."""
     R = len(recv_ex)
     ptrs = (vp * R)(*[None if t is None else t.data_ptr() for t in recv_ex])
     rows = (i64 * R)(*[int(r) for r in recv_rows])
-    _call("moe_ep_combine", pool.handle, int(T), buf, R, ptrs, rows, recv_start_dev.data_ptr(), y.data_ptr(),
-          moe._stream(stream))
+    _call("moe_ep_combine", pool.handle, int(T), buf, R, ptrs, rows,
+          None if recv_start_dev is None else recv_start_dev.data_ptr(),
+          None if copy_row is None else copy_row.data_ptr(), y.data_ptr(), moe._stream(stream))
 
 
 def dequant_rows(codes, scales, rows, out, stream=None):
@@ -285,6 +289,8 @@ class EmulatedGroup:
         self.recv_codes = [torch.empty((cap, H), dtype=torch.int8, device=device) for _ in range(R)]
         self.recv_scales = [torch.empty((cap, self.Gs), dtype=torch.float32, device=device) for _ in range(R)]
         self.recv_ex = [torch.empty((cap, H), dtype=torch.bfloat16, device=device) for _ in range(R)]
+        # where each rank's fused dispatch sent each copy (owner * 2^40 + row), for its fused combine
+        self.copy_rows = [torch.empty((T_max * k,), dtype=torch.int64, device=device) for _ in range(R)]
         self.error_word = torch.zeros(1, dtype=torch.int32, device=device)
         self._counts_host = torch.zeros((R, P), dtype=torch.int32).pin_memory()
         self._starts = torch.empty((R, P), dtype=torch.int32, device=device)
@@ -384,12 +390,15 @@ class EmulatedGroup:
         with torch.cuda.stream(s):
             return torch.from_numpy(tab).pin_memory().to(self.device, non_blocking=True)
 
-    def combine_fused(self, T_list, recv_rows, starts, ys=None, stream=None):
+    def combine_fused(self, T_list, recv_rows, starts, ys=None, stream=None, recorded=False):
         """Every rank's y straight from the owners' receive buffers (no
-        combine pull): moe_ep_combine per rank."""
+        combine pull): moe_ep_combine per rank.  With `recorded`, each copy's
+        row is the one the rank's fused dispatch recorded (dispatch_fused);
+        otherwise it is found from the plan and the window starts."""
         ys = ys or self._outputs(T_list, stream)
         self._per_rank(stream, lambda r, st: combine(self.pools[r], T_list[r], self.recv_ex, recv_rows, starts[r],
-                                                      ys[r], stream=st))
+                                                      ys[r], stream=st,
+                                                      copy_row=self.copy_rows[r] if recorded else None))
         return ys
 
     def plan_all(self, logits, rep_off=None, rep_ids=None, stream=None):
@@ -405,10 +414,11 @@ class EmulatedGroup:
         return self._starts, self._rows
 
     def dispatch_fused(self, xs, starts, stream=None):
-        """Every rank's fused dispatch into the owners' receive buffers."""
+        """Every rank's fused dispatch into the owners' receive buffers,
+        recording where each copy went (copy_rows)."""
         cap = [t.shape[0] for t in self.recv_codes]
         self._per_rank(stream, lambda r, st: dispatch(self.pools[r], xs[r], self.recv_codes, self.recv_scales, cap,
-                                                       starts[r], stream=st))
+                                                       starts[r], stream=st, copy_row=self.copy_rows[r]))
 
     def step(self, logits, xs, rep_off=None, rep_ids=None, recv_ex_out=None, stream=None, fused_combine=False,
              fused_dispatch=False):
@@ -456,7 +466,7 @@ class EmulatedGroup:
                 self.recv_ex[d][:recv_ex_out[d].shape[0]].copy_(recv_ex_out[d])
         cap = [t.shape[0] for t in self.recv_ex]
         T_list = [lg.shape[0] for lg in logits]
-        ys = self.combine_fused(T_list, cap, starts, stream=stream)
+        ys = self.combine_fused(T_list, cap, starts, stream=stream, recorded=True)
         counts = self.counts()
         if recv_rows is None:
             recv_rows = [int(v) for v in rows_dev.cpu().tolist()]
@@ -476,7 +486,7 @@ class EmulatedGroup:
             self.plan_all(logits, rep_off, rep_ids, s)
             starts, _ = self.starts_device(s)
             self.dispatch_fused(xs, starts, s)
-            self.combine_fused(T_list, cap, starts, ys=ys, stream=s)
+            self.combine_fused(T_list, cap, starts, ys=ys, stream=s, recorded=True)
 
         with torch.cuda.stream(s):
             body()  # warm (module loads, attributes) outside the capture

@@ -234,12 +234,15 @@ MOE_API int moe_ep_recv_start_device(int32_t R, int32_t P, const int32_t* const*
  *   recv_rows    host int64 [R]: rows each owner's buffers hold (bounds)
  *   recv_start   device int32 [P]: this rank's row of moe_ep_recv_start(_device),
  *                4-byte aligned
+ *   copy_row     device int64 [T, k] or NULL: where each copy went, recorded
+ *                for moe_ep_combine -- owner * 2^40 + row, or -1 for a copy
+ *                that was skipped; 8-byte aligned
  * A row outside its owner's buffer is skipped and sets MOE_DEVERR_UNIT.
  * Requires a prior moe_plan on this set with the same T.
  */
 MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, int32_t R,
                             int8_t* const* recv_codes, float* const* recv_scales, const int64_t* recv_rows,
-                            const int32_t* recv_start, void* stream);
+                            const int32_t* recv_start, int64_t* copy_row, void* stream);
 
 /*
  * Fused combine of rank s (a pull-mode reduction, StrataCL section 3.4:
@@ -257,12 +260,18 @@ MOE_API int moe_ep_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int bu
  *              expert outputs (NULL with 0 rows for a rank that owns none)
  *   recv_rows  host int64 [R]: rows of each owner's buffer (bounds)
  *   recv_start device int32 [P] (moe_ep_recv_start of rank s), 4-byte aligned
+ *   copy_row   device int64 [T, k] or NULL: the rows moe_ep_dispatch recorded
+ *              for this set and batch (then recv_start is not read and may be
+ *              NULL); with NULL each row is found from phys, offsets and
+ *              recv_start, one dependent load more per copy
  *   y          device bf16 [T, H]
- * A row outside its owner's buffer is skipped and sets MOE_DEVERR_UNIT in the
- * pool's error word.  Requires a prior moe_plan on this set with the same T.
+ * A row outside its owner's buffer (or a recorded -1) skips the token's
+ * segment and sets MOE_DEVERR_UNIT in the pool's error word.  Requires a
+ * prior moe_plan on this set with the same T.
  */
 MOE_API int moe_ep_combine(moe_pool* pool, int32_t T, int buf, int32_t R, const uint16_t* const* recv_ex,
-                           const int64_t* recv_rows, const int32_t* recv_start, uint16_t* y, void* stream);
+                           const int64_t* recv_rows, const int32_t* recv_start, const int64_t* copy_row,
+                           uint16_t* y, void* stream);
 
 /*
  * Dequantize rows (the identity-expert stand-in on any buffer, e.g. a

@@ -273,9 +273,9 @@ def test_fused_combine_checks_before_launch():
     ptrs = (ctypes.c_void_p * 2)(1 << 41, 1 << 41)
     rows = (ctypes.c_int64 * 2)(10, 10)
     good = ctypes.c_void_p(1 << 41)
-    assert L.moe_ep_combine(None, 8, 0, 2, ptrs, rows, good, good, None) == -1
-    assert L.moe_ep_combine(h, 8, 1, 2, ptrs, rows, good, good, None) == -4     # no set 1
-    assert L.moe_ep_combine(h, 65, 0, 2, ptrs, rows, good, good, None) == -2    # T > T_max
-    assert L.moe_ep_combine(h, 8, 0, 65, ptrs, rows, good, good, None) == -2    # R too large
-    assert L.moe_ep_combine(h, 8, 0, 2, ptrs, rows, good, good, None) == -9     # no plan on this set
+    assert L.moe_ep_combine(None, 8, 0, 2, ptrs, rows, good, None, good, None) == -1
+    assert L.moe_ep_combine(h, 8, 1, 2, ptrs, rows, good, None, good, None) == -4     # no set 1
+    assert L.moe_ep_combine(h, 65, 0, 2, ptrs, rows, good, None, good, None) == -2    # T > T_max
+    assert L.moe_ep_combine(h, 8, 0, 65, ptrs, rows, good, None, good, None) == -2    # R too large
+    assert L.moe_ep_combine(h, 8, 0, 2, ptrs, rows, good, None, good, None) == -9     # no plan on this set
     L.moe_pool_destroy(h)

@@ -224,6 +224,34 @@ def test_fused_combine_rejects_rows_outside_the_owners_buffers():
     assert int((y.view(torch.int16) != 0).sum().item()) == 0
 
 
+def test_recorded_rows_outside_the_owners_buffers_are_rejected():
+    """Recorded copy rows that are -1, name an owner outside the group, or
+    point past an owner's rows: the fused combine skips those tokens'
+    segments and reports MOE_DEVERR_UNIT; every other token is the oracle's."""
+    w = wl.dataclasses.replace(wl.small_variant(wl.WORKLOADS["t4096_h7168_e256p288_k8"], 64), H=256)
+    R = 2
+    inps = _inputs(w, R)
+    g = _group(w, R)
+    ys, counts, recv_rows = _run(g, inps, fused=True, fused_dispatch=True)
+    _check(g, inps, w, recv_rows, ys, counts, fused=True)
+    rec = g.copy_rows[0].view(w.T, w.k)
+    good = rec.clone()
+    rec[3, 0] = -1
+    rec[5, 1] = (R + 3) << 40                      # no such owner
+    rec[7, 2] = (1 << 40) + g.recv_ex[1].shape[0]  # one row past owner 1's buffer
+    y = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    cap = [t.shape[0] for t in g.recv_ex]
+    ep.combine(g.pools[0], w.T, g.recv_ex, cap, None, y, copy_row=g.copy_rows[0])
+    assert g.pools[0].check() & ep.DEVERR_UNIT
+    bad = {3, 5, 7}
+    yh = host_u16(y)
+    assert not yh[sorted(bad)].any()
+    keep = [t for t in range(w.T) if t not in bad]
+    np.testing.assert_array_equal(yh[keep], host_u16(ys[0])[keep])
+    g.pools[0].clear_error()
+    rec.copy_(good)
+
+
 def test_device_window_starts_equal_the_host_ones():
     """moe_ep_recv_start_device against moe_ep_recv_start and the rows each
     rank receives, at the bench shape and at a group with P < R."""
