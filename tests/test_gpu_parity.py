@@ -517,12 +517,13 @@ def test_cluster_plan_at_maximum_shapes(T):
     _custom(T, 128, E, P, 32, rng.standard_normal((T, E)), rep_off=off, rep_ids=ids, seed=T)
 
 
-@pytest.mark.parametrize("after_plan", [False, True])
-def test_bench_schedule_two_streams_full_size(after_plan):
+@pytest.mark.parametrize("mode", MODES)
+def test_bench_schedule_two_streams_full_size(mode):
     """The bench's timed schedule at the bench workload's full size: steps
     alternate the two buffer sets on two streams, launched back to back, each
     step with its own inputs and output buffer; every step's result is
-    checked against the oracle."""
+    checked against the oracle.  The bench's own form is moe_plan_dispatch
+    ("fused")."""
     w = wl.WORKLOADS["t4096_h7168_e256p288_k8"]
     pool = moe.Pool(w.T, w.H, w.E, w.P, w.k, n_sets=2)
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
@@ -539,8 +540,7 @@ def test_bench_schedule_two_streams_full_size(after_plan):
         s.wait_event(ev)
     for i, (_, logits, x, ex, ro, ri, y) in enumerate(steps):
         s, b = streams[i & 1], i & 1
-        pool.plan(logits, ro, ri, buf=b, stream=s)
-        pool.dispatch(x, buf=b, stream=s, after_plan=after_plan)
+        _plan_dispatch(pool, mode, logits, ro, ri, x, b, s)
         pool.combine(w.T, y=y, ex_out=ex, buf=b, stream=s)
     torch.cuda.synchronize()
     assert pool.check() == 0
