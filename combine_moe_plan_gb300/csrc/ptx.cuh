@@ -25,13 +25,6 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
                  : "memory");
 }
 
-// 16-byte store, streaming hint (evict-first: written once, read by a later kernel).
-__device__ __forceinline__ void st16_cs(void* p, uint4 v) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
-
 // bf16 halves of a 32-bit word -> fp32 (exact widening).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -81,10 +74,6 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 // nothing to the cluster, e.g. to say "done reading your shared memory".
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-    cluster_arrive();
-    cluster_wait();
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
