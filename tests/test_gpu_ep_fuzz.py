@@ -36,7 +36,7 @@ def _replica_map(rng, E):
     return P, np.array(off, np.int32), perm[np.array(ids)].astype(np.int32)
 
 
-@pytest.mark.parametrize("seed", range(150))
+@pytest.mark.parametrize("seed", range(500))
 def test_random_splits_match_oracle(seed):
     rng = np.random.default_rng(5000 + seed)
     R = int(rng.integers(1, 10))
