@@ -261,9 +261,12 @@ def rank_schedules(desc, counts_all, rank, H, scale_stride):
 
 class EmulatedGroup:
     """R ranks of an expert-parallel group on one GPU.  Rank r has its own
-    pool (moe.Pool, one buffer set) and a receive buffer sized for the worst
-    case (every rank sending every row to r: R * T_max * k rows); the two
-    exchanges each run as one moe_ep_pull launch over all R pullers.
+    pool (moe.Pool, one buffer set), a receive buffer sized for the worst case
+    (every rank sending every row to r: R * T_max * k rows) and a stream of its
+    own, on which its kernels run (forked from the caller's stream and joined
+    back to it).  Pulled exchanges run as one moe_ep_pull launch over all R
+    pullers; the fused forms run each rank's moe_ep_dispatch and
+    moe_ep_combine on its own stream.
 
     Every peer buffer is in this GPU's memory, so by default both tiers of the
     cost model are the local one (alpha 1 ns, 6000 GB/s) and no fan-out cap
