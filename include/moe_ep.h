@@ -32,7 +32,17 @@
  *   - moe_ep_pull executes the units: for one puller on a real group (its
  *     peers' buffers mapped into its address space), or for all R pullers
  *     of a group emulated on one GPU in one launch, with every rank's
- *     buffers in local memory.
+ *     buffers in local memory;
+ *   - or, fused (the write-up's direct writes into the receivers'
+ *     pre-allocated buffers): every (source, expert) window's first row in
+ *     its owner's buffer comes from every rank's counts (moe_ep_recv_start on
+ *     the host, moe_ep_recv_start_device without a trip to it);
+ *     moe_ep_dispatch quantizes a rank's tokens once and writes each copy
+ *     straight to its row in the owner's receive buffer, recording where it
+ *     went; moe_ep_combine reads each copy's expert output where its owner
+ *     holds it and reduces in ascending j into the rank's y (the reduction
+ *     form of StrataCL section 3.4).  No schedule and no pull; the receive
+ *     buffers and y are those of the pulled form, bit for bit.
  *
  * Conventions as in moe.h: 0 or a negative moe_status; arguments checked on
  * the host before anything is launched; device pointers 16-byte aligned;
@@ -50,8 +60,8 @@ extern "C" {
 
 #define MOE_EP_MAX_RANKS 64
 
-/* Device error-word bit (moe_ep_pull): a unit outside its buffers or an
- * out-of-range peer was skipped. */
+/* Device error-word bit (moe_ep_pull, moe_ep_dispatch, moe_ep_combine): a
+ * unit or a row outside its buffers, or an out-of-range peer, was skipped. */
 #define MOE_DEVERR_UNIT 0x8
 
 /*
