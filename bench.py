@@ -380,10 +380,17 @@ def decode_latency(dev, reps=200):
                     for l in range(n_chain)]
     chain_y = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(n_chain)]
 
-    def chain():
+    def chain(parts="layer"):
+        """16 consecutive layers: the whole layer, or only its plan, or its
+        plan and dispatch (what each part adds inside a chain)."""
         xin = x
         for l in range(n_chain):
+            if parts == "plan":
+                pool.plan(chain_logits[l], buf=l & 1, stream=s)
+                continue
             pool.plan_dispatch(chain_logits[l], xin, buf=l & 1, stream=s)
+            if parts == "plan+dispatch":
+                continue
             pool.combine(w.T, y=chain_y[l], buf=l & 1, stream=s)
             xin = chain_y[l]
 
@@ -404,6 +411,14 @@ def decode_latency(dev, reps=200):
     g_chain = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_chain, stream=s):
         chain()
+    g_parts = {}
+    for parts in ("plan", "plan+dispatch"):
+        with torch.cuda.stream(s):
+            chain(parts)
+        torch.cuda.synchronize()
+        g_parts[parts] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_parts[parts], stream=s):
+            chain(parts)
     torch.cuda.synchronize()
 
     def med(fn):
@@ -455,6 +470,7 @@ def decode_latency(dev, reps=200):
 
     layer_q = queued(g_layer.replay)
     chain_q = queued(g_chain.replay, n=50, spin=200000)
+    parts_q = {k: queued(g.replay, n=50, spin=200000)[3] / n_chain for k, g in g_parts.items()}
     # The floor of a graph of three kernels that do nothing (torch adds on 16
     # floats), queued the same way: what any three-kernel graph costs.
     tiny = torch.zeros(16, device=dev)
@@ -472,6 +488,8 @@ def decode_latency(dev, reps=200):
            "empty_three_kernel_graph_queued_us": empty_q[1],
            "empty_three_kernel_graph_queued_mean_us": empty_q[3],
            "layer_in_16_layer_graph_us": chain_q[3] / n_chain,
+           "parts_in_16_layer_graph_us": {"plan": parts_q["plan"], "plan+dispatch": parts_q["plan+dispatch"],
+                                          "plan+dispatch+combine": chain_q[3] / n_chain},
            "note": "CUDA-graph replays from an idle GPU; dispatch = plan + dispatch (the fused "
                    "dispatch carries the routing metadata); each graph launch adds its own overhead. "
                    "layer_queued: the same layer graph with its launch already queued behind a spin "
@@ -480,8 +498,9 @@ def decode_latency(dev, reps=200):
                    "a graph of three do-nothing kernels queued the same way (the graph's own cost); "
                    "layer_in_16_layer_graph: one replay of 16 consecutive layers (each its own logits, "
                    "its y the next layer's x) captured as one graph and queued the same way, mean over 50 "
-                   "replays divided by 16. Event timestamps tick in steps of about 1 us: the medians sit "
-                   "on steps, the means resolve finer"}
+                   "replays divided by 16; parts_in_16_layer_graph: the same chain of the plans alone and of "
+                   "the plans and dispatches, per layer. Event timestamps tick in steps of about 1 us: the "
+                   "medians sit on steps, the means resolve finer"}
     if pool.check() != 0:
         raise RuntimeError("device error word set in the decode-latency pass")
     return out
