@@ -9,7 +9,10 @@ group) and ep.rank_schedules (libmoe's layout and LPT schedules).  The
 schedules must equal the oracle's; executed on the host against every peer's
 rows (exchanged here by all-gathers that stand in for peer memory), the
 dispatch units must rebuild the oracle's receive buffer of the rank and the
-combine units its returned rows, and the rank's combine its local y.
+combine units its returned rows, and the rank's combine its local y.  The
+fused form's addressing (ep.recv_start, each copy written straight to its
+owner's row, the combine reading it there) must give the same receive buffer
+and the same y.
 """
 import multiprocessing as mp
 import os
@@ -115,6 +118,27 @@ def _worker(rank, ws, port, q):
         np.testing.assert_array_equal(ex_out, loc["ex_out"])
         y = oracle.combine(ex_out, pl["slot"], pl["gates"])
         np.testing.assert_array_equal(y, loc["y"])
+
+        # the fused form: this rank's window starts in every owner's buffer
+        # from every rank's counts (the product's host call), each copy
+        # written straight to row start[p] + slot - offsets[p] of its owner,
+        # and the combine reading each copy's expert row there
+        starts = np.asarray(ep.recv_start(counts_all, rank), np.int64)
+        slot_f, phys_f = pl["slot"].reshape(-1).astype(np.int64), pl["phys"].reshape(-1).astype(np.int64)
+        owner_f = (phys_f * ws) // w.P
+        dst_f = starts[phys_f] + slot_f - pl["offsets"][phys_f].astype(np.int64)
+        meta = _all_gather_rows(torch, dist, np.stack([owner_f, dst_f], 1))
+        payload = _all_gather_rows(torch, dist, codes[slot_f])
+        recv_fused = np.full((n_recv, w.H), 0x55, np.int8)
+        for mr, pr in zip(meta, payload):
+            mine = mr[:, 0] == rank
+            recv_fused[mr[mine, 1]] = pr[mine]
+        np.testing.assert_array_equal(recv_fused, recv_codes)
+        rows_f = np.stack([peers_ex[int(o)][int(d)] for o, d in zip(owner_f, dst_f)]) if len(dst_f) else \
+            np.zeros((0, w.H), np.uint16)
+        ex_f = np.zeros_like(ex_out)
+        ex_f[slot_f] = rows_f
+        np.testing.assert_array_equal(oracle.combine(ex_f, pl["slot"], pl["gates"]), loc["y"])
 
         # what each rank pulls from a peer is what that peer's window holds for it
         pulled = np.zeros(ws, np.int64)
