@@ -16,8 +16,6 @@ from __future__ import annotations
 import argparse
 import ctypes
 import json
-import os
-import sys
 
 import numpy as np
 

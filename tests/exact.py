@@ -5,7 +5,6 @@ arithmetic, round-to-nearest, ties-to-even, for a format with ``p`` significand
 bits (24 for binary32, 8 for bf16) and minimum normal exponent -126 (both).
 """
 from fractions import Fraction
-import math
 import struct
 
 import numpy as np

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from combine_moe_plan_gb300 import ep, moe
+from combine_moe_plan_gb300 import ep
 from combine_moe_plan_gb300 import workloads as wl
 from tests.gpu_util import assert_y_close, dev, dev_bf16, ensure_built, f32_bits, host_u16
 
