@@ -327,3 +327,39 @@ def test_fused_dispatch_rejects_rows_outside_the_owners_buffers():
     err = g.pools[0].check()
     assert err & ep.DEVERR_UNIT
     assert all(int(t.abs().sum().item()) == 0 for t in g.recv_codes)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_handworked_split_on_the_gpu(fused):
+    """The split worked by hand in tests/golden/ep_handworked.json, pulled and
+    fused: every owner receives the rows the fixture names, in its order (a
+    token's scale names it), the device window starts are the fixture's, and
+    every rank's y is the oracle's."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "ep_handworked.json")))
+    R, E, P, k, H = g["R"], g["E"], g["P"], g["k"], g["H"]
+    logits = [np.array(a, np.float32) for a in g["logits"]]
+    xs = []
+    for s in range(R):
+        x = np.zeros((len(g["logits"][s]), H), np.float32)
+        x[:, 0] = [1 + 4 * s + t for t in range(x.shape[0])]
+        xs.append(wl.f32_to_bf16_bits(x))
+    grp = ep.EmulatedGroup(R, 3, H, E, P, k, cores=2)
+    ys, counts, recv_rows = grp.step([dev(a) for a in logits], [dev_bf16(a) for a in xs],
+                                     fused_combine=fused, fused_dispatch=fused)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(counts, g["counts"])
+    assert list(recv_rows) == g["recv_rows"]
+    for d in range(R):
+        want = np.array([np.float32(1 + 4 * s + t) / np.float32(127) for s, t in g["received"][d]], np.float32)
+        got = grp.recv_scales[d][:recv_rows[d], 0].cpu().numpy()
+        np.testing.assert_array_equal(got.view(np.int32), want.view(np.int32))
+    starts, rows = grp.starts_device()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(starts.cpu().numpy(), g["recv_start"])
+    assert rows.cpu().tolist() == g["recv_rows"]
+    ref = oracle.ep_forward(logits, xs, k, P)
+    for s in range(R):
+        assert_y_close(host_u16(ys[s]), ref["y"][s], f"rank {s}")
+    assert grp.check() == 0

@@ -293,3 +293,41 @@ def test_hand_worked_schedules():
                 for u in r["units"][r["core_off"][c]:r["core_off"][c + 1]]] for c in range(case["C"])]
         assert got == case["core_units"], case["name"]
         assert r["makespan"] == case["makespan"], case["name"]
+
+
+def _handworked_split():
+    g = json.load(open(os.path.join(GOLDEN, "ep_handworked.json")))
+    R, H = g["R"], g["H"]
+    logits = [np.array(a, np.float32) for a in g["logits"]]
+    xs = []
+    for s in range(R):
+        x = np.zeros((len(g["logits"][s]), H), np.float32)
+        x[:, 0] = [1 + 4 * s + t for t in range(x.shape[0])]
+        xs.append(wl.f32_to_bf16_bits(x))
+    return g, logits, xs
+
+
+def test_handworked_split():
+    """The split worked by hand in tests/golden/ep_handworked.json: every
+    rank's plan, every owner's receive layout (window starts and rows), and
+    the order of the rows each owner receives (named by their scales)."""
+    g, logits, xs = _handworked_split()
+    R, P, k = g["R"], g["P"], g["k"]
+    for s in range(R):
+        pl = oracle.plan(logits[s], k, None, None, P)
+        np.testing.assert_array_equal(pl["topk_e"], g["topk_e"][s])
+        np.testing.assert_array_equal(pl["counts"], g["counts"][s])
+        np.testing.assert_array_equal(pl["offsets"], g["offsets"][s])
+        np.testing.assert_array_equal(pl["slot"], g["slot"][s])
+    counts = np.array(g["counts"], np.int32)
+    for d in range(R):
+        expert_off, chunk_row = oracle.ep_layout(counts, d)
+        assert int(expert_off[-1]) == g["recv_rows"][d]
+        mine = [p for p in range(P) if oracle.ep_owner(p, R, P) == d]
+        for i, p in enumerate(mine):
+            for s in range(R):
+                assert int(chunk_row[s, i]) == g["recv_start"][s][p]
+    ref = oracle.ep_forward(logits, xs, k, P)
+    for d in range(R):
+        want = np.array([np.float32(1 + 4 * s + t) / np.float32(127) for s, t in g["received"][d]], np.float32)
+        np.testing.assert_array_equal(ref["recv_scales"][d][:, 0].view(np.int32), want.view(np.int32))
