@@ -237,6 +237,8 @@ MOE_API int moe_dispatch(moe_pool* pool, const uint16_t* x, int32_t T, int buf, 
  * cannot check this: with any other kernel in between (one that writes x, or
  * one launched with programmatic dependent launch that triggers its
  * dependents early), use moe_dispatch.  Arguments and errors as moe_dispatch.
+ * moe_plan_dispatch gives the same early load with the precondition met by
+ * construction.
  */
 MOE_API int moe_dispatch_after_plan(moe_pool* pool, const uint16_t* x, int32_t T, int buf, void* stream);
 
