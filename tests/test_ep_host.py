@@ -279,3 +279,33 @@ def test_fused_combine_checks_before_launch():
     assert L.moe_ep_combine(h, 8, 0, 65, ptrs, rows, good, None, good, None) == -2    # R too large
     assert L.moe_ep_combine(h, 8, 0, 2, ptrs, rows, good, None, good, None) == -9     # no plan on this set
     L.moe_pool_destroy(h)
+
+
+def test_group_schedules_from_several_host_threads():
+    """Four host threads make group schedules at once: one holds the library's
+    worker threads, the others find them busy and compute on their own
+    thread; every result equals the single-puller schedules."""
+    import threading
+    errors = []
+
+    def run(seed):
+        try:
+            rng = np.random.default_rng(3000 + seed)
+            for _ in range(6):
+                R, P, counts, kw = _random_case(rng)
+                desc = ep.make_desc(R, P, kw["cores"], kw["fanout_cap"], kw["unit_rows"], kw["alpha_ns"],
+                                    kw["beta_gbs"])
+                units, core_off, _ = ep.schedule_group(desc, 1, counts, 2 * 7168)
+                want_u, want_off = ep.pack_schedules([ep.schedule(desc, 1, r, counts, 2 * 7168) for r in range(R)])
+                np.testing.assert_array_equal(units, want_u)
+                np.testing.assert_array_equal(core_off, want_off)
+        except Exception as e:  # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not any(t.is_alive() for t in threads)
+    assert not errors, errors
