@@ -125,6 +125,30 @@ def test_full_30720_in_full():
     assert run.err == 0
 
 
+def test_largest_batch_the_pool_takes():
+    """T = 2^20 tokens, the largest batch a pool takes (hidden 128, 64
+    experts with 16 replicas, top-8: 8.4 M copies, 32,768 route tiles):
+    the whole plan, every dispatch row and every combine output compared in
+    full with the oracle, through moe_plan_dispatch."""
+    T, H, E, k = 1 << 20, 128, 64, 8
+    rng = np.random.default_rng(77)
+    hot = rng.choice(E, size=16, replace=False)
+    off, ids, nxt = [0], [], E
+    for e in range(E):
+        mine = [e] + ([nxt] if e in hot else [])
+        nxt += e in hot
+        ids += mine
+        off.append(off[-1] + len(mine))
+    P = nxt
+    rep_off, rep_ids = np.array(off, np.int32), rng.permutation(P)[np.array(ids)].astype(np.int32)
+    w = wl.Workload("custom", T=T, H=H, E=E, P=P, k=k)
+    inp = {"logits": rng.standard_normal((T, E), dtype=np.float32),
+           "x": wl.f32_to_bf16_bits(rng.standard_normal((T, H), dtype=np.float32)),
+           "rep_off": rep_off, "rep_ids": rep_ids}
+    run = Run(w, inp, n_sets=1, fused=True)
+    _check_all(w, inp, run)
+
+
 # ------------------------------------------------------------ edge cases --
 
 def _custom(T, H, E, P, k, logits, x=None, rep_off=None, rep_ids=None, seed=0, T_max=None, pool=None):
