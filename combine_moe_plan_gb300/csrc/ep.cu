@@ -386,10 +386,13 @@ struct RecvTable {
     int64_t rows[MOE_EP_MAX_RANKS];
 };
 
-// Lane j < k of a warp holds copy j of token t: its owner's row address and
-// gate.  KB copies' 16-byte loads are in flight per lane before they are
-// accumulated in ascending j, as in the single-GPU combine.
-template <int KB, bool RECORDED>  // RECORDED: copy_row holds each copy's row
+// Lane j < k of a warp holds copy j of token t: its gate and its row's
+// address in its owner's buffer -- the row the rank's fused dispatch recorded
+// (RECORDED, one load), or recv_start[p] + slot - offsets[p] with p the
+// copy's physical expert (two dependent loads more).  KB copies' 16-byte
+// loads are in flight per lane before they are accumulated in ascending j,
+// as in the single-GPU combine.
+template <int KB, bool RECORDED>
 __global__ void __launch_bounds__(kCombineThreads)
 ep_combine_kernel(const int32_t* __restrict__ slot, const float* __restrict__ gates,
                   const int32_t* __restrict__ phys, const int32_t* __restrict__ offsets,
